@@ -1,0 +1,171 @@
+/*
+ * pagerank.h - C ABI of the GB300 (sm_103a) PageRank power-iteration library.
+ *
+ * The library computes PageRank by power iteration on one GPU:
+ *
+ *   x'[v] = (1 - d)/n + d * ( sum over in-neighbours u of x[u]/outdeg[u]
+ *                             + D/n ),     D = sum of x over dangling vertices
+ *
+ * ("Day 40 - PageRank on a real graph in CUDA", section "One iteration, three
+ * shapes of work", update formula; a dangling vertex is one with no out-edge,
+ * introduction of the same page), starting from x0 = 1/n (Meerkat, "Dynamic
+ * graph algorithms on GPUs", PageRank section, Algorithm 5, static case) and
+ * stopping after the first update whose L1 distance sum_v |x'[v] - x[v]| is
+ * below tol (same Meerkat section; Day 40, "Keep the dangling mass on the
+ * device").
+ *
+ * pr_graph_create transposes the caller's out-edge CSR into an in-edge CSR on
+ * the device (Day 40, "One iteration, three shapes of work": histogram, prefix
+ * sum, scatter) and splits the in-rows into in-degree classes (gpu-graph-study,
+ * "PageRank T4 - degree-bucketed load balancing": <= 32, 33..1024, > 1024).
+ * pr_run performs the whole iteration on the device inside one CUDA graph and
+ * synchronises the stream once, at the end.
+ *
+ * Conventions shared by every entry point:
+ *  - Vertex ids are int32 in [0, n); edge offsets are int64 on input and
+ *    int32 inside the library, so 1 <= n <= 2^31 - 2 and 0 <= m <= 2^31 - 1.
+ *  - A pointer argument may point to host memory (pageable or pinned) or to
+ *    device memory of the current device; the library tells them apart with
+ *    cudaPointerGetAttributes and copies as needed. Managed memory is treated
+ *    as device memory.
+ *  - `stream` is a cudaStream_t passed as void* (for example
+ *    torch.cuda.current_stream().cuda_stream); NULL means the legacy default
+ *    stream. All device work of a call is ordered on that stream.
+ *  - Every entry point that can fail returns a pr_status. Negative values are
+ *    errors: nothing is written to the caller's output buffers and
+ *    pr_last_error() returns a message (thread-local, valid until the next
+ *    call on the same thread). Calls on one pr_graph are not thread-safe.
+ */
+#ifndef PAGERANK_GB300_H
+#define PAGERANK_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle. Owns device memory: the in-edge CSR, per-vertex out-degrees,
+ * the in-degree class lists and, after the first pr_run of a precision, that
+ * precision's iteration state and its instantiated CUDA graph. */
+typedef struct pr_graph pr_graph;
+
+typedef enum pr_status {
+    PR_OK = 0,
+    PR_NOT_CONVERGED = 1,       /* tol > 0 and max_iter updates ran without L1 < tol;
+                                   ranks, iterations and L1 are still written */
+    PR_ERR_INVALID_ARG = -1,    /* bad scalar argument or NULL pointer */
+    PR_ERR_INVALID_GRAPH = -2,  /* row_ptr[0] != 0, row_ptr[n] != m, row_ptr
+                                   decreasing, or a col_idx entry outside [0, n) */
+    PR_ERR_TOO_LARGE = -3,      /* n or m beyond the int32 limits above */
+    PR_ERR_OOM = -4,            /* a device allocation failed */
+    PR_ERR_CUDA = -5,           /* any other CUDA runtime error */
+    PR_ERR_TIMEOUT = -6         /* a bounded device-side wait gave up (the
+                                   transpose's scan look-back); the context
+                                   stays usable, the handle is not created */
+} pr_status;
+
+typedef enum pr_dtype {
+    PR_F32 = 0,                 /* ranks and contributions in fp32, row sums in fp32
+                                   tree order, L1 and D totals in fp64 */
+    PR_F64 = 1                  /* everything in fp64 */
+} pr_dtype;
+
+/* Sizes of the preprocessed graph (filled by pr_graph_get_info). */
+typedef struct pr_graph_info {
+    int64_t n, m;
+    int64_t n_dangling;         /* vertices with out-degree 0 */
+    int64_t rows_zero;          /* in-degree 0: no gather */
+    int64_t rows_thread;        /* in-degree 1..32: one thread per row */
+    int64_t rows_warp;          /* in-degree 33..1024: one warp per row */
+    int64_t rows_cta;           /* in-degree > 1024: split into chunks, one CTA per chunk */
+    int64_t edges_thread, edges_warp, edges_cta;
+    int64_t cta_chunks;         /* number of CTA chunks */
+    int32_t cta_chunk_edges;    /* edges per CTA chunk (the last one of a row may be shorter) */
+    int32_t iterate_grid;       /* CTAs of the persistent iteration kernel */
+    int64_t device_bytes;       /* device memory held by the handle */
+    int32_t build_launches;     /* kernels pr_graph_create launched */
+} pr_graph_info;
+
+/* Statistics of the most recent pr_run on a handle (filled by pr_graph_last_run). */
+typedef struct pr_run_stats {
+    int32_t iterations;         /* updates performed */
+    int32_t converged;          /* 1 if the last update had L1 < tol (tol > 0) */
+    double l1;                  /* L1 distance of the last update */
+    double dangling_mass;       /* D of the final vector */
+    float loop_ms;              /* device time of the iteration loop alone (CUDA events
+                                   recorded on the run's stream around the graph launch) */
+    float total_ms;             /* device time from the first to the last kernel of pr_run */
+    int32_t launches;           /* kernels pr_run launched (init, one per update, output) */
+} pr_run_stats;
+
+/*
+ * Builds the device-side graph from an out-edge CSR.
+ *   n        number of vertices (1 <= n <= 2^31 - 2)
+ *   m        number of edges (0 <= m <= 2^31 - 1)
+ *   row_ptr  int64[n + 1], row_ptr[0] = 0, non-decreasing, row_ptr[n] = m;
+ *            the out-edges of u are col_idx[row_ptr[u] .. row_ptr[u+1])
+ *   col_idx  int32[m], targets in [0, n); duplicates and self-loops are kept
+ *            and count with their multiplicity; may be NULL when m = 0
+ *   out      receives the handle on success (untouched on failure)
+ * Inputs are borrowed for the duration of the call only: the caller may free
+ * or overwrite them once it returns (the call synchronises `stream`).
+ * Returns PR_OK, PR_ERR_INVALID_ARG, PR_ERR_INVALID_GRAPH, PR_ERR_TOO_LARGE,
+ * PR_ERR_OOM, PR_ERR_TIMEOUT or PR_ERR_CUDA.
+ */
+pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
+                          const int32_t *col_idx, void *stream, pr_graph **out);
+
+/*
+ * Runs the power iteration on a graph.
+ *   d          damping factor, 0 <= d <= 1
+ *   tol        L1 tolerance; the run stops after the first update with
+ *              L1 < tol. tol <= 0 runs exactly max_iter updates.
+ *   max_iter   cap on the number of updates, >= 1
+ *   dtype      PR_F32 or PR_F64: the precision of the iteration and of
+ *              ranks_out and x_init
+ *   ranks_out  n values of dtype, written with the final ranks
+ *              (caller-owned, host or device)
+ *   x_init     NULL for the uniform start 1/n, else n values of dtype used
+ *              as the start vector (warm start); not renormalised
+ *   iters_out  optional (NULL): number of updates performed
+ *   l1_out     optional (NULL): L1 distance of the last update
+ * The whole loop runs on the device; the call synchronises `stream` once,
+ * at the end. Returns PR_OK, PR_NOT_CONVERGED, or an error.
+ */
+pr_status pr_run(pr_graph *g, double d, double tol, int32_t max_iter,
+                 pr_dtype dtype, void *ranks_out, const void *x_init,
+                 int32_t *iters_out, double *l1_out, void *stream);
+
+/*
+ * Copies the in-edge CSR out of the handle (for verification).
+ *   in_ptr  int32[n + 1]: the in-edges of v are in_col[in_ptr[v] .. in_ptr[v+1])
+ *   in_col  int32[m]: the sources, ascending within each row (the order of
+ *           a stable counting sort by destination); may be NULL when m = 0
+ * Buffers are caller-owned, host or device. Synchronises `stream`.
+ */
+pr_status pr_get_in_csr(const pr_graph *g, int32_t *in_ptr, int32_t *in_col,
+                        void *stream);
+
+/* Fills *info with the sizes of the preprocessed graph. */
+pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info);
+
+/* Fills *stats with the statistics of the handle's most recent pr_run. */
+pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
+
+/* Frees the handle and all device memory it owns. NULL is ignored. The
+ * caller must make sure no work using the handle is still in flight on a
+ * stream other than the ones its calls already synchronised. */
+void pr_graph_destroy(pr_graph *g);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char *pr_last_error(void);
+
+/* Library version string. */
+const char *pr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGERANK_GB300_H */

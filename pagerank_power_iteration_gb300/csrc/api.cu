@@ -1,0 +1,295 @@
+// The C ABI (include/pagerank.h): argument checks, host/device pointer
+// handling, ownership of device memory, and error reporting. The compute is
+// in transpose.cu (pr_graph_create) and iterate.cu (pr_run).
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "pr_internal.cuh"
+
+#define PR_API extern "C" __attribute__((visibility("default")))
+
+namespace prk {
+
+static thread_local char g_last_error[512] = "";
+
+pr_status set_error(pr_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pr_status cuda_status(cudaError_t e, const char *what)
+{
+    cudaGetLastError();   // clear a non-sticky error
+    return set_error(e == cudaErrorMemoryAllocation ? PR_ERR_OOM : PR_ERR_CUDA, "%s: %s (%s)",
+                     what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+pr_status graph_alloc(pr_graph *g, void **p, size_t bytes)
+{
+    if (bytes == 0)
+        bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        cudaGetLastError();
+        return set_error(e == cudaErrorMemoryAllocation ? PR_ERR_OOM : PR_ERR_CUDA,
+                         "cudaMalloc of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+    }
+    g->allocs.push_back(*p);
+    g->device_bytes += (int64_t)bytes;
+    return PR_OK;
+}
+
+bool is_device_pointer(const void *p)
+{
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+}
+
+}  // namespace prk
+
+namespace {
+
+constexpr int64_t kMaxN = ((int64_t)1 << 31) - 2;
+constexpr int64_t kMaxM = ((int64_t)1 << 31) - 1;
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            cudaGetLastError();
+            prev = -1;
+        }
+        if (dev >= 0 && dev != prev)
+            cudaSetDevice(dev);
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0)
+            cudaSetDevice(prev);
+    }
+};
+
+void free_graph(pr_graph *g)
+{
+    if (!g)
+        return;
+    prk::release_dtype_state(g);
+    for (cudaEvent_t &ev : g->ev)
+        if (ev)
+            cudaEventDestroy(ev);
+    for (void *p : g->allocs)
+        cudaFree(p);
+    if (g->h_scal)
+        cudaFreeHost(g->h_scal);
+    delete g;
+}
+
+}  // namespace
+
+using prk::set_error;
+
+PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
+                                 const int32_t *col_idx, void *stream, pr_graph **out)
+{
+    if (out == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "out is NULL");
+    if (n < 1)
+        return set_error(PR_ERR_INVALID_ARG, "n must be >= 1 (got %lld)", (long long)n);
+    if (m < 0)
+        return set_error(PR_ERR_INVALID_ARG, "m must be >= 0 (got %lld)", (long long)m);
+    if (n > kMaxN)
+        return set_error(PR_ERR_TOO_LARGE, "n = %lld exceeds 2^31 - 2", (long long)n);
+    if (m > kMaxM)
+        return set_error(PR_ERR_TOO_LARGE, "m = %lld exceeds 2^31 - 1", (long long)m);
+    if (row_ptr == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "row_ptr is NULL");
+    if (m > 0 && col_idx == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "col_idx is NULL but m > 0");
+
+    cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return prk::cuda_status(e, "cudaGetDevice");
+
+    pr_graph *g = new (std::nothrow) pr_graph();
+    if (!g)
+        return set_error(PR_ERR_OOM, "host allocation failed");
+    g->n = n;
+    g->m = m;
+    g->device = dev;
+    pr_status st = PR_OK;
+
+    do {
+        e = cudaDeviceGetAttribute(&g->num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) { st = prk::cuda_status(e, "device query"); break; }
+        for (cudaEvent_t &ev : g->ev) {
+            e = cudaEventCreate(&ev);
+            if (e != cudaSuccess) break;
+        }
+        if (e != cudaSuccess) { st = prk::cuda_status(e, "cudaEventCreate"); break; }
+        e = cudaMallocHost((void **)&g->h_scal, sizeof(prk::Scalars));
+        if (e != cudaSuccess) { st = prk::cuda_status(e, "cudaMallocHost"); break; }
+        if ((st = prk::graph_alloc(g, (void **)&g->scal, sizeof(prk::Scalars))) != PR_OK) break;
+        if ((st = prk::graph_alloc(g, (void **)&g->err, sizeof(unsigned))) != PR_OK) break;
+        e = cudaMemsetAsync(g->scal, 0, sizeof(prk::Scalars), s);
+        if (e != cudaSuccess) { st = prk::cuda_status(e, "memset"); break; }
+
+        // inputs on the device (borrowed, or staged copies freed below)
+        const bool rp_dev = prk::is_device_pointer(row_ptr);
+        const bool ci_dev = (m == 0) || prk::is_device_pointer(col_idx);
+        int64_t ends[2];
+        if (rp_dev) {
+            e = cudaMemcpyAsync(&ends[0], row_ptr, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(&ends[1], row_ptr + n, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
+            if (e == cudaSuccess)
+                e = cudaStreamSynchronize(s);
+            if (e != cudaSuccess) { st = prk::cuda_status(e, "reading row_ptr"); break; }
+        } else {
+            ends[0] = row_ptr[0];
+            ends[1] = row_ptr[n];
+        }
+        if (ends[0] != 0) {
+            st = set_error(PR_ERR_INVALID_GRAPH, "row_ptr[0] = %lld, expected 0", (long long)ends[0]);
+            break;
+        }
+        if (ends[1] != m) {
+            st = set_error(PR_ERR_INVALID_GRAPH, "row_ptr[n] = %lld, expected m = %lld",
+                           (long long)ends[1], (long long)m);
+            break;
+        }
+        void *rp_stage = nullptr, *ci_stage = nullptr;
+        const int64_t *d_rp = row_ptr;
+        const int32_t *d_ci = col_idx;
+        if (!rp_dev) {
+            e = cudaMalloc(&rp_stage, (size_t)(n + 1) * sizeof(int64_t));
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(rp_stage, row_ptr, (size_t)(n + 1) * sizeof(int64_t),
+                                    cudaMemcpyHostToDevice, s);
+            d_rp = (const int64_t *)rp_stage;
+        }
+        if (e == cudaSuccess && !ci_dev) {
+            e = cudaMalloc(&ci_stage, (size_t)m * sizeof(int32_t));
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(ci_stage, col_idx, (size_t)m * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, s);
+            d_ci = (const int32_t *)ci_stage;
+        }
+        if (e != cudaSuccess) {
+            st = prk::cuda_status(e, "staging the input CSR");
+        } else {
+            st = prk::build_graph(g, d_rp, d_ci, s);
+        }
+        cudaError_t se = cudaStreamSynchronize(s);
+        if (rp_stage)
+            cudaFree(rp_stage);
+        if (ci_stage)
+            cudaFree(ci_stage);
+        if (st == PR_OK && se != cudaSuccess)
+            st = prk::cuda_status(se, "pr_graph_create");
+    } while (0);
+
+    if (st != PR_OK) {
+        free_graph(g);
+        return st;
+    }
+    *out = g;
+    return PR_OK;
+}
+
+PR_API pr_status pr_run(pr_graph *g, double d, double tol, int32_t max_iter, pr_dtype dtype,
+                        void *ranks_out, const void *x_init, int32_t *iters_out, double *l1_out,
+                        void *stream)
+{
+    if (g == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "graph is NULL");
+    if (!(d >= 0.0 && d <= 1.0))
+        return set_error(PR_ERR_INVALID_ARG, "d must be in [0, 1] (got %g)", d);
+    if (tol != tol)
+        return set_error(PR_ERR_INVALID_ARG, "tol is NaN");
+    if (max_iter < 1)
+        return set_error(PR_ERR_INVALID_ARG, "max_iter must be >= 1 (got %d)", (int)max_iter);
+    if (dtype != PR_F32 && dtype != PR_F64)
+        return set_error(PR_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (ranks_out == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "ranks_out is NULL");
+    DeviceGuard guard(g->device);
+    return prk::run(g, d, tol, max_iter, (int)dtype, ranks_out, x_init, iters_out, l1_out,
+                    (cudaStream_t)stream);
+}
+
+PR_API pr_status pr_get_in_csr(const pr_graph *g, int32_t *in_ptr, int32_t *in_col, void *stream)
+{
+    if (g == nullptr || in_ptr == nullptr || (g->m > 0 && in_col == nullptr))
+        return set_error(PR_ERR_INVALID_ARG, "NULL argument");
+    DeviceGuard guard(g->device);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(in_ptr, g->in_ptr, (size_t)(g->n + 1) * sizeof(int32_t),
+                                    cudaMemcpyDefault, s);
+    if (e == cudaSuccess && g->m > 0)
+        e = cudaMemcpyAsync(in_col, g->in_col, (size_t)g->m * sizeof(int32_t), cudaMemcpyDefault, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    return e == cudaSuccess ? PR_OK : prk::cuda_status(e, "pr_get_in_csr");
+}
+
+PR_API pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info)
+{
+    if (g == nullptr || info == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "NULL argument");
+    memset(info, 0, sizeof(*info));
+    info->n = g->n;
+    info->m = g->m;
+    info->n_dangling = g->n_dangling;
+    info->rows_zero = g->n_z;
+    info->rows_thread = g->n_t;
+    info->rows_warp = g->n_w;
+    info->rows_cta = g->n_c;
+    info->edges_thread = g->e_t;
+    info->edges_warp = g->e_w;
+    info->edges_cta = g->e_c;
+    info->cta_chunks = g->n_chunks;
+    info->cta_chunk_edges = prk::kChunkEdges;
+    info->iterate_grid = g->st[0].ready ? g->st[0].grid : g->st[1].grid;
+    info->device_bytes = g->device_bytes;
+    info->build_launches = g->build_launches;
+    return PR_OK;
+}
+
+PR_API pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats)
+{
+    if (g == nullptr || stats == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "NULL argument");
+    *stats = g->last;
+    return PR_OK;
+}
+
+PR_API void pr_graph_destroy(pr_graph *g)
+{
+    if (!g)
+        return;
+    DeviceGuard guard(g->device);
+    free_graph(g);
+}
+
+PR_API const char *pr_last_error(void) { return prk::g_last_error; }
+
+PR_API const char *pr_version(void) { return "pagerank-gb300 0.1 (sm_103a)"; }

@@ -1,0 +1,114 @@
+// Internal declarations shared by the library's translation units.
+// Not part of the ABI: callers use include/pagerank.h only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "pagerank.h"
+
+namespace prk {
+
+// In-degree classes of the pull SpMV (gpu-graph-study, "PageRank T4 -
+// degree-bucketed load balancing": thread per row up to 32, warp per row up
+// to 1024, block per row above). Rows above kWarpMax are cut into chunks of
+// kChunkEdges edges so that one hub is spread over many CTAs.
+constexpr int kThreadMax = 32;
+constexpr int kWarpMax = 1024;
+constexpr int kChunkEdges = 4096;
+constexpr int kBlock = 256;
+
+enum RowClass : int { kClassZero = 0, kClassThread = 1, kClassWarp = 2, kClassCta = 3 };
+
+// Bits of the device error word.
+enum : unsigned {
+    kErrRowPtr = 1u,    // row_ptr decreases somewhere
+    kErrColIdx = 2u,    // a col_idx entry is outside [0, n)
+    kErrTimeout = 4u,   // a bounded look-back wait gave up
+};
+
+// Device-resident scalars of a run. Written by the init kernel, read at the
+// start of every update and rewritten by the last CTA of each update.
+struct Scalars {
+    double dmass;       // dangling mass D of the current vector
+    double l1;          // L1 distance of the last update
+    double d;           // damping factor
+    double tol;         // L1 tolerance (<= 0: fixed number of updates)
+    double inv_n;       // 1/n
+    int32_t it;         // updates performed so far
+    int32_t max_iter;
+    int32_t converged;
+    uint32_t ticket;    // arrival counter for the last-CTA reductions
+};
+
+// Per-precision iteration state of a handle.
+struct DtypeState {
+    bool ready = false;
+    void *s[2] = {nullptr, nullptr};   // ping-pong state: x/outdeg, or x for dangling
+    void *hub_partial = nullptr;       // one partial row sum per CTA chunk
+    void *stage = nullptr;             // staging for host x_init / ranks_out
+    double *block_partials = nullptr;  // [grid][2]: L1 and D partial of each CTA
+    int grid = 0;                      // CTAs of the persistent iteration kernel
+    int init_grid = 0;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace prk
+
+struct pr_graph {
+    int64_t n = 0, m = 0;
+    int device = 0;
+    int num_sms = 0;
+
+    // in-edge CSR and per-vertex data
+    int32_t *in_ptr = nullptr;     // [n + 1]
+    int32_t *in_col = nullptr;     // [m], 16-byte aligned
+    int32_t *deg_out = nullptr;    // [n]
+
+    // in-degree classes
+    int32_t *rows_z = nullptr, *rows_t = nullptr, *rows_w = nullptr, *rows_c = nullptr;
+    int32_t *chunk_row = nullptr;   // [n_chunks]: index into rows_c
+    int32_t *chunk_first = nullptr; // [n_c + 1]: first chunk of each CTA row
+    uint32_t *hub_arrivals = nullptr; // [n_c]: chunks of the row finished this update
+    int64_t n_dangling = 0, n_z = 0, n_t = 0, n_w = 0, n_c = 0, n_chunks = 0;
+    int64_t e_t = 0, e_w = 0, e_c = 0;
+
+    prk::Scalars *scal = nullptr;   // device
+    unsigned *err = nullptr;        // device error word
+    prk::Scalars *h_scal = nullptr; // pinned host mirror
+
+    prk::DtypeState st[2];
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    pr_run_stats last = {};
+
+    int32_t build_launches = 0;     // kernels launched by pr_graph_create
+    std::vector<void *> allocs;     // every device allocation owned by the handle
+    int64_t device_bytes = 0;
+};
+
+namespace prk {
+
+// Error reporting (api.cu).
+pr_status set_error(pr_status st, const char *fmt, ...);
+pr_status cuda_status(cudaError_t e, const char *what);
+
+// Device allocation owned by the handle (api.cu).
+pr_status graph_alloc(pr_graph *g, void **p, size_t bytes);
+
+// True if p can be dereferenced by the current device as device memory.
+bool is_device_pointer(const void *p);
+
+// Transpose + classification (transpose.cu). d_row_ptr/d_col are device pointers.
+pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col,
+                      cudaStream_t s);
+
+// Iteration (iterate.cu).
+pr_status run(pr_graph *g, double d, double tol, int32_t max_iter, int dtype,
+              void *ranks_out, const void *x_init, int32_t *iters_out, double *l1_out,
+              cudaStream_t s);
+void release_dtype_state(pr_graph *g);
+
+}  // namespace prk

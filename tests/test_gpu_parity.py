@@ -1,0 +1,226 @@
+"""Parity of the CUDA path (through the C ABI) against the oracle.
+
+The transpose must be bit-exact. Ranks are compared at the same number of
+updates (the oracle is rerun with that fixed count); converged iteration
+counts must agree within one update.
+"""
+import numpy as np
+import pytest
+
+import graphgen as gg
+import oracle
+from conftest import day40_case
+from gpu_util import F32, F64, assert_ranks_close
+
+torch = pytest.importorskip("torch")
+import pagerank_power_iteration_gb300 as prg  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+D = 0.85
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "the GPU tests need a CUDA device"
+    from pagerank_power_iteration_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def graph(name):
+    if name in ("tiny", "single", "nodangling", "dangling", "star", "chain"):
+        return day40_case(name)
+    if name == "star_out":
+        return gg.star_out(10000)
+    if name == "no_edges":
+        return gg.from_edges(5, [], [])
+    if name == "all_dangling_but_one":
+        return gg.from_edges(300, [7, 7], [3, 250])
+    if name == "selfloops1":
+        return gg.from_edges(1, [0, 0, 0], [0, 0, 0])
+    if name == "dups_loops":
+        return gg.random_sparse(3000, 40000, seed=11, dangling_frac=0.3)
+    if name == "hub70k":
+        return gg.star_in(70000)
+    if name == "n257":
+        return gg.random_sparse(257, 3000, seed=3)
+    if name == "n65537":
+        return gg.random_sparse(65537, 300000, seed=4, dangling_frac=0.1)
+    if name == "citation30k":
+        return gg.workload("citation30k")
+    if name == "rmat14":
+        return gg.rmat(14, seed=6)
+    if name == "rmat18":
+        return gg.workload("rmat18")
+    if name == "er16":
+        return gg.erdos_renyi(1 << 16, 16, 0.1, seed=5)
+    raise KeyError(name)
+
+
+SMALL = ["tiny", "single", "nodangling", "dangling", "star", "chain", "star_out", "no_edges",
+         "all_dangling_but_one", "selfloops1", "dups_loops", "hub70k", "n257", "n65537",
+         "citation30k", "rmat14", "er16"]
+
+
+@pytest.mark.parametrize("name", SMALL + ["rmat18"])
+def test_transpose_bit_exact(name):
+    rp, ci = graph(name)
+    with prg.Graph(rp, ci) as g:
+        ip, ic = g.in_csr()
+        info = g.info()
+    oip, oic = oracle.transpose(rp, ci)
+    assert np.array_equal(ip.astype(np.int64), oip)
+    assert np.array_equal(ic, oic)
+    indeg = np.diff(oip)
+    assert info["rows_zero"] == int((indeg == 0).sum())
+    assert info["rows_thread"] == int(((indeg >= 1) & (indeg <= 32)).sum())
+    assert info["rows_warp"] == int(((indeg > 32) & (indeg <= 1024)).sum())
+    assert info["rows_cta"] == int((indeg > 1024).sum())
+    assert info["edges_cta"] == int(indeg[indeg > 1024].sum())
+    assert info["n_dangling"] == int((np.diff(rp) == 0).sum())
+
+
+def _parity(rp, ci, dtype, tol=1e-6, max_iter=200, check_iters=True):
+    tt = {"f32": torch.float32, "f64": torch.float64}[dtype]
+    tolset = F32 if dtype == "f32" else F64
+    with prg.Graph(rp, ci) as g:
+        x, it, l1, conv = g.run(D, tol, max_iter, dtype=tt)
+        x = x.cpu().numpy()
+    ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=it)
+    assert_ranks_close(x, ref["x"], tolset, f"{dtype} after {it} updates")
+    assert abs(x.sum() - 1.0) <= tolset["sum"]
+    assert abs(l1 - ref["l1"]) <= max(0.02 * ref["l1"], 2e-7 if dtype == "f32" else 1e-12)
+    if check_iters and tol > 0:
+        refc = oracle.pagerank(rp, ci, D, tol=tol, max_iter=max_iter)
+        assert abs(refc["iters"] - it) <= 1, (refc["iters"], it)
+        assert conv == (refc["status"] == oracle.OK) or abs(refc["iters"] - it) == 1
+    return it
+
+
+@pytest.mark.parametrize("name", SMALL + ["rmat18"])
+def test_converged_ranks_f32(name):
+    rp, ci = graph(name)
+    _parity(rp, ci, "f32")
+
+
+@pytest.mark.parametrize("name", ["tiny", "dangling", "star", "chain", "dups_loops", "hub70k",
+                                  "citation30k", "rmat14", "er16"])
+def test_converged_ranks_f64(name):
+    rp, ci = graph(name)
+    _parity(rp, ci, "f64", tol=1e-10, max_iter=400)
+
+
+@pytest.mark.parametrize("name", ["dangling", "citation30k", "rmat14"])
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_fixed_iterations(name, dtype):
+    """tol <= 0 runs exactly max_iter updates (the timed fixed-50 mode)."""
+    rp, ci = graph(name)
+    tt = {"f32": torch.float32, "f64": torch.float64}[dtype]
+    for k in (1, 2, 50):
+        with prg.Graph(rp, ci) as g:
+            x, it, l1, conv = g.run(D, 0.0, k, dtype=tt)
+        assert it == k and conv
+        ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=k)
+        assert_ranks_close(x.cpu().numpy(), ref["x"], F32 if dtype == "f32" else F64, f"k={k}")
+
+
+def test_closed_forms_on_device():
+    """Cycle: 1/n after one update; star (leaves -> centre): the closed form."""
+    rp, ci = gg.cycle(100000)
+    with prg.Graph(rp, ci) as g:
+        x, it, l1, conv = g.run(D, 1e-6, 200)
+    assert it == 1 and conv
+    assert np.allclose(x.cpu().numpy(), 1.0 / 100000, rtol=1e-6, atol=0)
+    k = 10000
+    rp, ci = gg.star_in(k)
+    with prg.Graph(rp, ci) as g:
+        x, it, l1, conv = g.run(D, 1e-9, 500, dtype=torch.float64)
+    xc = (1 + k * D) / (1 + k + k * D)
+    assert abs(x[0].item() - xc) < 1e-9
+
+
+@pytest.mark.parametrize("d", [0.0, 0.5, 1.0])
+def test_damping_extremes(d):
+    rp, ci = graph("dangling")
+    with prg.Graph(rp, ci) as g:
+        x, it, l1, conv = g.run(d, 0.0, 20, dtype=torch.float64)
+    ref = oracle.pagerank(rp, ci, d, tol=0.0, max_iter=20)
+    assert_ranks_close(x.cpu().numpy(), ref["x"], F64, f"d={d}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_warm_start(dtype):
+    rp, ci = graph("citation30k")
+    tt = {"f32": torch.float32, "f64": torch.float64}[dtype]
+    rng = np.random.default_rng(3)
+    x0 = rng.random(len(rp) - 1)
+    x0 /= x0.sum()
+    with prg.Graph(rp, ci) as g:
+        xi = torch.tensor(x0, dtype=tt, device="cuda")
+        x, it, l1, conv = g.run(D, 0.0, 7, dtype=tt, x_init=xi)
+        xh, _, _, _ = g.run(D, 0.0, 7, dtype=tt, x_init=x0.astype(np.float32 if dtype == "f32" else np.float64))
+    ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=7, x_init=x0)
+    tol = F32 if dtype == "f32" else F64
+    assert_ranks_close(x.cpu().numpy(), ref["x"], tol, "device x_init")
+    assert_ranks_close(xh.cpu().numpy(), ref["x"], tol, "host x_init")
+
+
+def test_host_and_device_buffers_agree():
+    rp, ci = graph("rmat14")
+    with prg.Graph(rp, ci) as g:                      # host inputs
+        xa, ita, _, _ = g.run(D, 1e-6, 200)
+        host_out = np.empty(len(rp) - 1, dtype=np.float32)
+        xb, itb, _, _ = g.run(D, 1e-6, 200, out=host_out)
+    rpd = torch.from_numpy(rp).cuda()
+    cid = torch.from_numpy(ci).cuda()
+    with prg.Graph(rpd, cid) as g:                    # device inputs
+        xc, itc, _, _ = g.run(D, 1e-6, 200)
+    assert ita == itb == itc
+    assert xb is host_out
+    assert np.array_equal(xa.cpu().numpy(), host_out)
+    assert np.array_equal(xa.cpu().numpy(), xc.cpu().numpy())
+
+
+def test_runs_are_repeatable_and_reusable():
+    rp, ci = graph("rmat18")
+    with prg.Graph(rp, ci) as g:
+        a, ita, l1a, _ = g.run(D, 1e-6, 200)
+        b, itb, l1b, _ = g.run(D, 1e-6, 200)
+        c, itc, _, _ = g.run(D, 0.0, 5, dtype=torch.float64)
+        e, ite, l1e, _ = g.run(D, 1e-6, 200)
+        st = g.last_run()
+    assert ita == itb == ite and itc == 5
+    np.testing.assert_allclose(a.cpu().numpy(), b.cpu().numpy(), rtol=1e-6, atol=0)
+    np.testing.assert_allclose(a.cpu().numpy(), e.cpu().numpy(), rtol=1e-6, atol=0)
+    assert st["iterations"] == ite and st["loop_ms"] > 0
+
+
+def test_not_converged_status():
+    rp, ci = graph("citation30k")
+    with prg.Graph(rp, ci) as g:
+        x, it, l1, conv = g.run(D, 1e-12, 3)
+    assert it == 3 and not conv and l1 > 1e-12
+
+
+def test_invalid_graphs_are_rejected():
+    rp, ci = graph("tiny")
+    bad = ci.copy(); bad[3] = 6
+    with pytest.raises(prg.PageRankError) as e:
+        prg.Graph(rp, bad)
+    assert e.value.status == prg.PR_ERR_INVALID_GRAPH
+    bad = ci.copy(); bad[0] = -2
+    with pytest.raises(prg.PageRankError) as e:
+        prg.Graph(torch.from_numpy(rp).cuda(), torch.from_numpy(bad).cuda())
+    assert e.value.status == prg.PR_ERR_INVALID_GRAPH
+    rbad = rp.copy(); rbad[2], rbad[3] = rbad[3], rbad[2]
+    with pytest.raises(prg.PageRankError) as e:
+        prg.Graph(rbad, ci)
+    assert e.value.status == prg.PR_ERR_INVALID_GRAPH
+    rbad = rp.copy(); rbad[-1] -= 1
+    with pytest.raises(prg.PageRankError) as e:
+        prg.Graph(rbad, ci)
+    assert e.value.status == prg.PR_ERR_INVALID_GRAPH
+    # the context is still usable afterwards
+    with prg.Graph(rp, ci) as g:
+        x, it, _, _ = g.run(D, 1e-6, 100)
+    assert it > 1
