@@ -78,10 +78,11 @@ typedef struct pr_graph_info {
     int64_t rows_zero;          /* in-degree 0: no gather */
     int64_t rows_thread;        /* in-degree 1..32: one thread per row */
     int64_t rows_warp;          /* in-degree 33..1024: one warp per row */
-    int64_t rows_cta;           /* in-degree > 1024: split into chunks, one CTA per chunk */
+    int64_t rows_cta;           /* in-degree > 1024: split into chunks streamed by CTAs */
     int64_t edges_thread, edges_warp, edges_cta;
     int64_t cta_chunks;         /* number of CTA chunks */
-    int32_t cta_chunk_edges;    /* edges per CTA chunk (the last one of a row may be shorter) */
+    int32_t cta_chunk_edges;    /* edges per chunk of a CTA row, one warp each (the last
+                                   chunk of a row may be shorter) */
     int32_t iterate_grid;       /* CTAs of the persistent iteration kernel */
     int64_t device_bytes;       /* device memory held by the handle */
     int32_t build_launches;     /* kernels pr_graph_create launched */

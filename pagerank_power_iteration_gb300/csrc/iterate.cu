@@ -10,10 +10,14 @@
 //     written by the update that produced x[u] (the contribution cache of
 //     Meerkat's PageRank, Algorithm 5, and "Precomputed inverse out-degree" of
 //     gpu-graph-study's T3 tier);
-//   - the pull SpMV over the in-edge CSR gathers s, by in-degree class:
-//     one thread per row (<= 32 in-edges), one warp per row (33..1024), and
-//     CTA-sized chunks of 4096 edges for larger rows, whose partial sums the
-//     CTA finishing the row's last chunk adds up in chunk order;
+//   - the pull SpMV gathers s over the class-major work CSR (the in-edge CSR
+//     relabelled so that each in-degree class is one contiguous range of rows
+//     and edges, see transpose.cu), by class: rows above 1024 in-edges are
+//     streamed by whole CTAs, 512 edges per warp, whose partial sums the warp
+//     finishing the row's last chunk adds up in chunk order (no CTA-wide
+//     barrier); one warp per row for 33..1024;
+//     one thread per row for 1..32; rows without in-edges take the constant
+//     term only. CTA and warp rows are padded to whole 16-byte index loads;
 //   - the combine reads D from device memory (Day 40, "Keep the dangling mass
 //     on the device"), writes s' and accumulates the L1 distance and the next
 //     dangling mass;
@@ -39,17 +43,19 @@ namespace {
 
 template <typename T>
 struct IterArgs {
-    const int32_t *in_ptr;
-    const int32_t *in_col;
-    const int32_t *deg_out;
-    const int32_t *rows_z, *rows_t, *rows_w, *rows_c;
+    const int32_t *w_ptr;     // work CSR offsets (class-major order)
+    const int32_t *w_col;     // work sources; padding entries point at slot n
+    const int32_t *w_deg;     // out-degrees in work order
     const int32_t *chunk_row, *chunk_first;
     uint32_t *hub_arrivals;
-    T *s0, *s1;
+    T *s0, *s1;               // state [n + 1], slot n is 0
     T *hub_partial;
     double *block_partials;
     Scalars *scal;
-    int64_t n, n_z, n_t, n_w, n_chunks;
+    const int32_t *perm;      // vertex id -> work position (start vector, output)
+    const int32_t *order;     // work position -> vertex id
+    const int32_t *deg_out;   // out-degrees by vertex id
+    int64_t n, n_c, n_w, n_t, n_z, n_chunks;
 };
 
 // streaming (evict-first) loads of the index stream
@@ -81,79 +87,53 @@ __device__ __forceinline__ T block_sum(T v, T *red)
     return t;
 }
 
-// Sum of s[in_col[j]] for j in [b, e) over `lanes` cooperating threads
-// (`lane` in [0, lanes)): an unaligned head of at most 3 edges, a body of
-// 16-byte index loads, and a tail of at most 3 edges.
-template <typename T, int kLanes>
-__device__ __forceinline__ T gather_range(const int32_t *__restrict__ col, const T *__restrict__ s,
-                                          int64_t b, int64_t e, int lane)
-{
-    T acc0 = T(0), acc1 = T(0);
-    const int64_t a0 = (b + 3) & ~int64_t(3);
-    const int64_t a1 = e & ~int64_t(3);
-    if (a0 >= a1) {
-        for (int64_t j = b + lane; j < e; j += kLanes)
-            acc0 += __ldg(s + ld_stream(col + j));
-        return acc0;
+// The gathered state: slots below `hot` come from the CTA's shared-memory
+// copy of the head of the state vector, the rest from global memory.
+template <typename T>
+struct Gather {
+    const T *__restrict__ s;   // global state (s_old)
+    const T *h;                // shared copy of s[0, hot)
+    int32_t hot;
+    __device__ __forceinline__ T operator()(int32_t u) const
+    {
+        return u < hot ? h[u] : __ldg(s + u);
     }
-    if (b + lane < a0)
-        acc0 += __ldg(s + ld_stream(col + b + lane));
-    if (a1 + lane < e)
-        acc1 += __ldg(s + ld_stream(col + a1 + lane));
-    const int4 *cv = reinterpret_cast<const int4 *>(col + a0);
-    const int64_t nv = (a1 - a0) >> 2;
-    int64_t k = lane;
-    for (; k + kLanes < nv; k += 2 * kLanes) {
-        const int4 q = ld_stream4(cv + k);
-        const int4 r = ld_stream4(cv + k + kLanes);
-        acc0 += __ldg(s + q.x);
-        acc1 += __ldg(s + q.y);
-        acc0 += __ldg(s + q.z);
-        acc1 += __ldg(s + q.w);
-        acc0 += __ldg(s + r.x);
-        acc1 += __ldg(s + r.y);
-        acc0 += __ldg(s + r.z);
-        acc1 += __ldg(s + r.w);
+    __device__ __forceinline__ T four(int4 q) const
+    {
+        return ((*this)(q.x) + (*this)(q.y)) + ((*this)(q.z) + (*this)(q.w));
     }
-    if (k < nv) {
-        const int4 q = ld_stream4(cv + k);
-        acc0 += __ldg(s + q.x);
-        acc1 += __ldg(s + q.y);
-        acc0 += __ldg(s + q.z);
-        acc1 += __ldg(s + q.w);
-    }
-    return acc0 + acc1;
-}
+};
 
 __device__ __forceinline__ float abs_t(float x) { return fabsf(x); }
 __device__ __forceinline__ double abs_t(double x) { return ::fabs(x); }
 
-// The combine for one row: new rank, new state, L1 and dangling-mass terms.
+// The combine for work row i: new rank, new state, L1 and dangling-mass terms.
 template <typename T>
-__device__ __forceinline__ void finish_row(int32_t v, T y, const int32_t *__restrict__ deg_out,
+__device__ __forceinline__ void finish_row(int64_t i, T y, const int32_t *__restrict__ w_deg,
                                            const T *__restrict__ s_old, T *__restrict__ s_new,
                                            T base, T d, T &l1, T &dm)
 {
-    const int32_t deg = deg_out[v];
-    const T so = s_old[v];
+    const int32_t deg = w_deg[i];
+    const T so = s_old[i];
     const T x_old = deg ? so * T(deg) : so;
     const T x_new = base + d * y;
     l1 += abs_t(x_new - x_old);
     if (deg) {
-        __stcs(s_new + v, x_new / T(deg));
+        __stcs(s_new + i, x_new / T(deg));
     } else {
-        __stcs(s_new + v, x_new);
+        __stcs(s_new + i, x_new);
         dm += x_new;
     }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kBlock)
-k_iterate(IterArgs<T> a, cudaGraphConditionalHandle cond)
+__global__ void __launch_bounds__(kIterBlock, 1)
+k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
 {
-    __shared__ T s_red[32];
+    extern __shared__ __align__(16) unsigned char s_dyn[];
     __shared__ double s_redd[32];
     __shared__ int s_flag;
+    constexpr int kWarps = kIterBlock / 32;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t G = gridDim.x;
@@ -168,66 +148,157 @@ k_iterate(IterArgs<T> a, cudaGraphConditionalHandle cond)
     const T d = T(dd);
     const T base = T((1.0 - dd) * inv_n + dd * D * inv_n);
 
+    // the head of the state vector, where the work order puts the most
+    // gathered vertices, staged in shared memory for this update
+    T *s_hot = reinterpret_cast<T *>(s_dyn);
+    for (int32_t u = tid; u < hot; u += kIterBlock)
+        s_hot[u] = s_old[u];
+    __syncthreads();
+    const Gather<T> gat{s_old, s_hot, hot};
+
     T l1 = T(0), dm = T(0);
 
-    // rows with more than 1024 in-edges, in chunks of kChunkEdges
-    for (int64_t c = blockIdx.x; c < a.n_chunks; c += G) {
-        const int32_t r = a.chunk_row[c];
-        const int32_t v = a.rows_c[r];
-        const int32_t first = a.chunk_first[r];
-        const int32_t nch = a.chunk_first[r + 1] - first;
-        const int64_t rb = a.in_ptr[v], re = a.in_ptr[v + 1];
-        const int64_t cb = rb + (int64_t)(c - first) * kChunkEdges;
-        const int64_t ce = min(cb + (int64_t)kChunkEdges, re);
-        T part = gather_range<T, kBlock>(a.in_col, s_old, cb, ce, tid);
-        part = block_sum(part, s_red);
-        if (tid == 0) {
-            __stcg(a.hub_partial + c, part);
-            __threadfence();
-            const uint32_t prev = atomicAdd(a.hub_arrivals + r, 1u);
-            s_flag = (prev == (uint32_t)(nch - 1));
+    // CTA class: rows with more than 1024 in-edges, cut into chunks of
+    // kChunkEdges (16-byte aligned, whole int4s). A CTA's warps take
+    // consecutive chunks, so a CTA streams kChunkEdges * 8 consecutive edges
+    // of a hub, but every warp reduces and hands off its own chunk: no
+    // CTA-wide barrier. The warp that finishes a row's last chunk adds the
+    // row's chunk partials in chunk order and combines the row.
+    {
+        const int64_t nwarps = G * kWarps;
+        const int4 *cv_all = reinterpret_cast<const int4 *>(a.w_col);
+        constexpr int kVecPerLane = kChunkEdges / 4 / 32;
+        for (int64_t c = (int64_t)blockIdx.x * kWarps + warp; c < a.n_chunks; c += nwarps) {
+            const int32_t r = a.chunk_row[c];
+            const int32_t first = a.chunk_first[r];
+            const int32_t nch = a.chunk_first[r + 1] - first;
+            const int64_t cb = a.w_ptr[r] + (int64_t)(c - first) * kChunkEdges;
+            const int64_t ce = min(cb + (int64_t)kChunkEdges, (int64_t)a.w_ptr[r + 1]);
+            const int nv = (int)((ce - cb) >> 2);
+            const int4 *cv = cv_all + (cb >> 2);
+            int4 q[kVecPerLane];
+#pragma unroll
+            for (int t = 0; t < kVecPerLane; ++t)
+                if (lane + 32 * t < nv)
+                    q[t] = ld_stream4(cv + lane + 32 * t);
+            T part = T(0);
+#pragma unroll
+            for (int t = 0; t < kVecPerLane; ++t)
+                if (lane + 32 * t < nv)
+                    part += gat.four(q[t]);
+            part = warp_sum(part);
+            uint32_t prev = 0;
+            if (lane == 0) {
+                __stcg(a.hub_partial + c, part);
+                __threadfence();
+                prev = atomicAdd(a.hub_arrivals + r, 1u);
+            }
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev == (uint32_t)(nch - 1)) {
+                __threadfence();
+                T y = T(0);
+                for (int32_t k = lane; k < nch; k += 32)
+                    y += __ldcg(a.hub_partial + first + k);
+                y = warp_sum(y);
+                if (lane == 0) {
+                    a.hub_arrivals[r] = 0u;
+                    finish_row(r, y, a.w_deg, s_old, s_new, base, d, l1, dm);
+                }
+            }
         }
-        __syncthreads();
-        if (s_flag && tid == 0) {
-            __threadfence();
-            T y = T(0);
-            for (int32_t k = 0; k < nch; ++k)
-                y += __ldcg(a.hub_partial + first + k);
-            a.hub_arrivals[r] = 0u;
-            finish_row(v, y, a.deg_out, s_old, s_new, base, d, l1, dm);
-        }
-        __syncthreads();
     }
 
-    // 33..1024 in-edges: one warp per row
-    for (int64_t i = (int64_t)blockIdx.x * (kBlock / 32) + warp; i < a.n_w; i += G * (kBlock / 32)) {
-        const int32_t v = a.rows_w[i];
-        T y = gather_range<T, 32>(a.in_col, s_old, a.in_ptr[v], a.in_ptr[v + 1], lane);
-        y = warp_sum(y);
-        if (lane == 0)
-            finish_row(v, y, a.deg_out, s_old, s_new, base, d, l1, dm);
-    }
-
-    // 1..32 in-edges: one thread per row
-    for (int64_t i = (int64_t)blockIdx.x * kBlock + tid; i < a.n_t; i += G * kBlock) {
-        const int32_t v = a.rows_t[i];
-        const int32_t b = a.in_ptr[v], e = a.in_ptr[v + 1];
-        T y0 = T(0), y1 = T(0);
-        int32_t j = b;
-        for (; j + 1 < e; j += 2) {
-            const int32_t u0 = ld_stream(a.in_col + j);
-            const int32_t u1 = ld_stream(a.in_col + j + 1);
-            y0 += __ldg(s_old + u0);
-            y1 += __ldg(s_old + u1);
+    // warp class: one warp per row, 33..1024 in-edges (16-byte aligned,
+    // whole int4s). A warp takes 32 consecutive rows, reads their offsets in
+    // one coalesced load, walks them four rows at a time so that each lane
+    // has up to 16 gathers in flight, and finally combines row q in lane q.
+    {
+        const int64_t w0 = a.n_c, w1 = a.n_c + a.n_w;
+        const int64_t batches = (a.n_w + 31) / 32;
+        const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
+        for (int64_t bi = (int64_t)blockIdx.x * kWarps + warp; bi < batches; bi += G * kWarps) {
+            const int64_t r0 = w0 + bi * 32;
+            const int cnt = (int)min((int64_t)32, w1 - r0);
+            int32_t rb = 0, re = 0;
+            if (lane < cnt) {
+                rb = a.w_ptr[r0 + lane];
+                re = a.w_ptr[r0 + lane + 1];
+            }
+            T mine = T(0);
+            for (int q0 = 0; q0 < cnt; q0 += 4) {
+                int32_t b4[4], l4[4];
+                int32_t lmax = 0;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int32_t b = __shfl_sync(0xffffffffu, rb, (q0 + t) & 31);
+                    const int32_t e = __shfl_sync(0xffffffffu, re, (q0 + t) & 31);
+                    b4[t] = b >> 2;
+                    l4[t] = (q0 + t < cnt) ? ((e - b) >> 2) : 0;
+                    lmax = max(lmax, l4[t]);
+                }
+                T y[4] = {T(0), T(0), T(0), T(0)};
+                for (int32_t k = lane; k < lmax; k += 32) {
+                    int4 v[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (k < l4[t])
+                            v[t] = ld_stream4(cv + b4[t] + k);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (k < l4[t])
+                            y[t] += gat.four(v[t]);
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const T sum = warp_sum(y[t]);
+                    if (lane == q0 + t)
+                        mine = sum;
+                }
+            }
+            if (lane < cnt)
+                finish_row(r0 + lane, mine, a.w_deg, s_old, s_new, base, d, l1, dm);
         }
-        if (j < e)
-            y0 += __ldg(s_old + ld_stream(a.in_col + j));
-        finish_row(v, y0 + y1, a.deg_out, s_old, s_new, base, d, l1, dm);
     }
 
-    // no in-edges
-    for (int64_t i = (int64_t)blockIdx.x * kBlock + tid; i < a.n_z; i += G * kBlock)
-        finish_row(a.rows_z[i], T(0), a.deg_out, s_old, s_new, base, d, l1, dm);
+    // thread class: one thread per row, 1..32 in-edges; each thread walks two
+    // rows at once, two edges of each per step (missing edges gather the zero
+    // slot n), so four independent gathers are in flight
+    {
+        const int64_t t0 = a.n_c + a.n_w, t1 = t0 + a.n_t, stride = G * kIterBlock;
+        const int32_t zero_slot = (int32_t)a.n;
+        for (int64_t i = t0 + (int64_t)blockIdx.x * kIterBlock + tid; i < t1; i += 2 * stride) {
+            const int64_t i2 = i + stride;
+            const bool two = i2 < t1;
+            const int32_t b0 = a.w_ptr[i], e0 = a.w_ptr[i + 1];
+            const int32_t b1 = two ? a.w_ptr[i2] : 0, e1 = two ? a.w_ptr[i2 + 1] : 0;
+            T y0 = T(0), y1 = T(0), y2 = T(0), y3 = T(0);
+            const int32_t steps = max(e0 - b0, e1 - b1);
+            for (int32_t k = 0; k < steps; k += 2) {
+                const int32_t u0 = (b0 + k < e0) ? ld_stream(a.w_col + b0 + k) : zero_slot;
+                const int32_t u1 = (b0 + k + 1 < e0) ? ld_stream(a.w_col + b0 + k + 1) : zero_slot;
+                const int32_t u2 = (b1 + k < e1) ? ld_stream(a.w_col + b1 + k) : zero_slot;
+                const int32_t u3 = (b1 + k + 1 < e1) ? ld_stream(a.w_col + b1 + k + 1) : zero_slot;
+                y0 += gat(u0);
+                y1 += gat(u1);
+                y2 += gat(u2);
+                y3 += gat(u3);
+            }
+            finish_row(i, y0 + y1, a.w_deg, s_old, s_new, base, d, l1, dm);
+            if (two)
+                finish_row(i2, y2 + y3, a.w_deg, s_old, s_new, base, d, l1, dm);
+        }
+    }
+
+    // rows without in-edges: x' = base; four rows per thread in flight
+    {
+        const int64_t z0 = a.n - a.n_z, stride = G * kIterBlock;
+        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < a.n; i += 4 * stride) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                if (i + t * stride < a.n)
+                    finish_row(i + t * stride, T(0), a.w_deg, s_old, s_new, base, d, l1, dm);
+        }
+    }
 
     // reductions: one fp64 partial pair per CTA, the last CTA sums them
     const double l1_blk = block_sum((double)l1, s_redd);
@@ -244,7 +315,7 @@ k_iterate(IterArgs<T> a, cudaGraphConditionalHandle cond)
         return;
     __threadfence();
     double L = 0.0, M = 0.0;
-    for (int64_t b = tid; b < G; b += kBlock) {
+    for (int64_t b = tid; b < G; b += kIterBlock) {
         L += __ldcg(a.block_partials + 2 * b);
         M += __ldcg(a.block_partials + 2 * b + 1);
     }
@@ -265,8 +336,8 @@ k_iterate(IterArgs<T> a, cudaGraphConditionalHandle cond)
     }
 }
 
-// Start vector (1/n, or the caller's x_init), its state and dangling mass,
-// and the run scalars.
+// Start vector (1/n, or the caller's x_init in vertex ids), its state in
+// work order and its dangling mass, and the run scalars.
 template <typename T>
 __global__ void __launch_bounds__(kBlock)
 k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_t max_iter)
@@ -277,13 +348,17 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
     const int64_t G = gridDim.x;
     const T x_uniform = T(1.0 / (double)a.n);
     T dm = T(0);
-    for (int64_t v = (int64_t)blockIdx.x * kBlock + tid; v < a.n; v += G * kBlock) {
-        const T x = x_init ? x_init[v] : x_uniform;
-        const int32_t deg = a.deg_out[v];
+    if (blockIdx.x == 0 && tid == 0) {
+        a.s0[a.n] = T(0);   // the zero slot gathered by padding entries
+        a.s1[a.n] = T(0);
+    }
+    for (int64_t i = (int64_t)blockIdx.x * kBlock + tid; i < a.n; i += G * kBlock) {
+        const T x = x_init ? x_init[a.order[i]] : x_uniform;
+        const int32_t deg = a.w_deg[i];
         if (deg) {
-            a.s0[v] = x / T(deg);
+            a.s0[i] = x / T(deg);
         } else {
-            a.s0[v] = x;
+            a.s0[i] = x;
             dm += x;
         }
     }
@@ -316,7 +391,8 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
     }
 }
 
-// Ranks from the final state: x = s * outdeg, or s for a dangling vertex.
+// Ranks from the final state, in vertex ids: x[v] = s[perm[v]] * outdeg[v],
+// or s[perm[v]] for a dangling vertex.
 template <typename T>
 __global__ void k_output(IterArgs<T> a, T *__restrict__ out)
 {
@@ -325,7 +401,7 @@ __global__ void k_output(IterArgs<T> a, T *__restrict__ out)
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < a.n;
          v += (int64_t)gridDim.x * blockDim.x) {
         const int32_t deg = a.deg_out[v];
-        const T sv = s[v];
+        const T sv = s[a.perm[v]];
         out[v] = deg ? sv * T(deg) : sv;
     }
 }
@@ -335,13 +411,9 @@ IterArgs<T> make_args(pr_graph *g)
 {
     DtypeState &st = g->st[sizeof(T) == 8 ? 1 : 0];
     IterArgs<T> a;
-    a.in_ptr = g->in_ptr;
-    a.in_col = g->in_col;
-    a.deg_out = g->deg_out;
-    a.rows_z = g->rows_z;
-    a.rows_t = g->rows_t;
-    a.rows_w = g->rows_w;
-    a.rows_c = g->rows_c;
+    a.w_ptr = g->w_ptr;
+    a.w_col = g->w_col;
+    a.w_deg = g->w_deg;
     a.chunk_row = g->chunk_row;
     a.chunk_first = g->chunk_first;
     a.hub_arrivals = g->hub_arrivals;
@@ -350,10 +422,14 @@ IterArgs<T> make_args(pr_graph *g)
     a.hub_partial = (T *)st.hub_partial;
     a.block_partials = st.block_partials;
     a.scal = g->scal;
+    a.perm = g->perm;
+    a.order = g->order;
+    a.deg_out = g->deg_out;
     a.n = g->n;
-    a.n_z = g->n_z;
-    a.n_t = g->n_t;
+    a.n_c = g->n_c;
     a.n_w = g->n_w;
+    a.n_t = g->n_t;
+    a.n_z = g->n_z;
     a.n_chunks = g->n_chunks;
     return a;
 }
@@ -367,20 +443,28 @@ pr_status prepare(pr_graph *g)
     if (st.ready)
         return PR_OK;
     pr_status r;
+    const int64_t hot_cap = kHotBytes / (int64_t)sizeof(T);
+    st.hot = (int32_t)(g->n + 1 < hot_cap ? g->n + 1 : hot_cap);
+    st.smem = (size_t)st.hot * sizeof(T);
+    cudaError_t e = cudaFuncSetAttribute(k_iterate<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)st.smem);
+    if (e != cudaSuccess)
+        return cuda_status(e, "shared memory attribute");
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_iterate<T>, kBlock, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_iterate<T>, kIterBlock, st.smem);
     if (e != cudaSuccess)
         return cuda_status(e, "occupancy query");
     if (per_sm < 1)
-        per_sm = 1;
+        return set_error(PR_ERR_CUDA, "the update kernel does not fit on an SM");
     st.grid = per_sm * g->num_sms;
-    st.init_grid = st.grid;
+    st.init_grid = 8 * g->num_sms;
     const size_t n = (size_t)g->n;
-    if ((r = graph_alloc(g, &st.s[0], n * sizeof(T))) != PR_OK) return r;
-    if ((r = graph_alloc(g, &st.s[1], n * sizeof(T))) != PR_OK) return r;
+    if ((r = graph_alloc(g, &st.s[0], (n + 1) * sizeof(T))) != PR_OK) return r;
+    if ((r = graph_alloc(g, &st.s[1], (n + 1) * sizeof(T))) != PR_OK) return r;
     if ((r = graph_alloc(g, &st.stage, n * sizeof(T))) != PR_OK) return r;
     if ((r = graph_alloc(g, &st.hub_partial, (size_t)(g->n_chunks + 1) * sizeof(T))) != PR_OK) return r;
-    if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)st.grid * 2 * sizeof(double))) != PR_OK)
+    const int pgrid = st.grid > st.init_grid ? st.grid : st.init_grid;
+    if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)pgrid * 2 * sizeof(double))) != PR_OK)
         return r;
 
     IterArgs<T> args = make_args<T>(g);
@@ -390,7 +474,8 @@ pr_status prepare(pr_graph *g)
     cudaGraphNodeParams cp = {};
     cudaGraphNode_t cnode, knode;
     cudaKernelNodeParams kp = {};
-    void *kargs[] = {&args, &handle};
+    int32_t hot = st.hot;
+    void *kargs[] = {&args, &hot, &handle};
 
     e = cudaGraphCreate(&graph, 0);
     if (e == cudaSuccess)
@@ -405,8 +490,8 @@ pr_status prepare(pr_graph *g)
     if (e == cudaSuccess) {
         kp.func = (void *)k_iterate<T>;
         kp.gridDim = dim3((unsigned)st.grid);
-        kp.blockDim = dim3(kBlock);
-        kp.sharedMemBytes = 0;
+        kp.blockDim = dim3(kIterBlock);
+        kp.sharedMemBytes = (unsigned)st.smem;
         kp.kernelParams = kargs;
         e = cudaGraphAddKernelNode(&knode, cp.conditional.phGraph_out[0], nullptr, 0, &kp);
     }

@@ -14,11 +14,14 @@ namespace prk {
 // In-degree classes of the pull SpMV (gpu-graph-study, "PageRank T4 -
 // degree-bucketed load balancing": thread per row up to 32, warp per row up
 // to 1024, block per row above). Rows above kWarpMax are cut into chunks of
-// kChunkEdges edges so that one hub is spread over many CTAs.
+// kChunkEdges edges, one warp each, so that a CTA streams 8 consecutive
+// chunks and one hub is spread over many CTAs.
 constexpr int kThreadMax = 32;
 constexpr int kWarpMax = 1024;
-constexpr int kChunkEdges = 4096;
-constexpr int kBlock = 256;
+constexpr int kChunkEdges = 512;
+constexpr int kBlock = 256;        // CTA size of the preprocessing kernels
+constexpr int kIterBlock = 1024;   // CTA size of the update kernel (one CTA per SM)
+constexpr int kHotBytes = 160 * 1024;   // shared-memory copy of the state's head
 
 enum RowClass : int { kClassZero = 0, kClassThread = 1, kClassWarp = 2, kClassCta = 3 };
 
@@ -46,12 +49,15 @@ struct Scalars {
 // Per-precision iteration state of a handle.
 struct DtypeState {
     bool ready = false;
-    void *s[2] = {nullptr, nullptr};   // ping-pong state: x/outdeg, or x for dangling
+    void *s[2] = {nullptr, nullptr};   // ping-pong state [n + 1] in work order: x/outdeg,
+                                       // or x for a dangling vertex; slot n stays 0
     void *hub_partial = nullptr;       // one partial row sum per CTA chunk
     void *stage = nullptr;             // staging for host x_init / ranks_out
     double *block_partials = nullptr;  // [grid][2]: L1 and D partial of each CTA
     int grid = 0;                      // CTAs of the persistent iteration kernel
     int init_grid = 0;
+    int32_t hot = 0;                   // state slots staged in shared memory per update
+    size_t smem = 0;                   // dynamic shared memory of the update kernel
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
 };
@@ -63,15 +69,24 @@ struct pr_graph {
     int device = 0;
     int num_sms = 0;
 
-    // in-edge CSR and per-vertex data
+    // in-edge CSR in the caller's vertex ids (kept for pr_get_in_csr)
     int32_t *in_ptr = nullptr;     // [n + 1]
-    int32_t *in_col = nullptr;     // [m], 16-byte aligned
-    int32_t *deg_out = nullptr;    // [n]
+    int32_t *in_col = nullptr;     // [m]
+    int32_t *deg_out = nullptr;    // [n] out-degrees, caller's ids
 
-    // in-degree classes
-    int32_t *rows_z = nullptr, *rows_t = nullptr, *rows_w = nullptr, *rows_c = nullptr;
-    int32_t *chunk_row = nullptr;   // [n_chunks]: index into rows_c
-    int32_t *chunk_first = nullptr; // [n_c + 1]: first chunk of each CTA row
+    // work layout: the graph relabelled in class-major order (CTA rows, warp
+    // rows, thread rows, rows without in-edges; ascending ids in a class)
+    int32_t *order = nullptr;      // [n] work position -> vertex id
+    int32_t *perm = nullptr;       // [n] vertex id -> work position
+    int32_t *w_ptr = nullptr;      // [n + 1] work CSR offsets; CTA and warp rows padded
+                                   // to a multiple of 4 edges (16-byte aligned)
+    int32_t *w_col = nullptr;      // [m_w] work sources; padding entries point at slot n
+    int32_t *w_deg = nullptr;      // [n] out-degrees in work order
+    int64_t m_w = 0;               // edges in the work CSR, padding included
+
+    // CTA rows (work rows [0, n_c)) are cut into chunks of kChunkEdges edges
+    int32_t *chunk_row = nullptr;    // [n_chunks]: work row of each chunk
+    int32_t *chunk_first = nullptr;  // [n_c + 1]: first chunk of each CTA row
     uint32_t *hub_arrivals = nullptr; // [n_c]: chunks of the row finished this update
     int64_t n_dangling = 0, n_z = 0, n_t = 0, n_w = 0, n_c = 0, n_chunks = 0;
     int64_t e_t = 0, e_w = 0, e_c = 0;

@@ -1,28 +1,48 @@
-// One-time preprocessing on the device: out-edge CSR -> in-edge CSR, and the
-// split of in-rows into in-degree classes.
+// One-time preprocessing on the device: out-edge CSR -> in-edge CSR, the split
+// of in-rows into in-degree classes, and the class-major work layout the
+// iteration runs on.
 //
 // The transpose is the counting sort of "Day 40 - PageRank on a real graph in
 // CUDA" (section "One iteration, three shapes of work": a histogram, a prefix
 // sum and a scatter), done on the GPU:
-//   1. k_outdeg     out-degrees, row_ptr validation, dangling count
-//   2. k_expand     source id of every edge, col_idx validation, and the
-//                   in-degree histogram (global atomics)
-//   3. k_scan_excl  in_ptr = exclusive prefix sum of the in-degrees, one pass
-//                   with decoupled look-back between tiles
-//   4. the stable scatter, as a least-significant-digit radix sort of the
-//      edges by destination with 8-bit digits: each pass is itself a counting
-//      sort over 256 bins (per-tile shared-memory digit counts, decoupled
-//      look-back across tiles, rank-preserving scatter), so the edges into
-//      one vertex keep the order of the out-edge CSR, i.e. ascending sources.
-//      A 2^24-vertex graph needs 3 passes; a single counting sort over n bins
+//   1. k_outdeg      out-degrees, row_ptr validation, dangling count
+//   2. k_digit_hist  col_idx validation and the 256-bin digit counts of every
+//                    radix pass (one read of the edges)
+//   3. the stable scatter, as a least-significant-digit radix sort of the
+//      edges by destination with 8-bit digits (k_radix_pass). Each pass is
+//      itself a counting sort over 256 bins: per-warp shared-memory digit
+//      counts, decoupled look-back across tiles, and a rank-preserving scatter
+//      staged through shared memory so that the stores are coalesced. Stable
+//      passes keep the edges into one vertex in out-edge CSR order, i.e. with
+//      ascending sources. The first pass derives each edge's source from
+//      row_ptr as it loads the edge; the last pass also produces the
+//      in-degree histogram, one atomic per run of equal destinations in a
+//      tile. A 2^24-vertex graph takes 3 passes: one counting sort over n bins
 //      would need n-entry histograms that no shared memory holds.
-// Then k_scan_excl over class flags and k_compact build the row lists of the
-// four in-degree classes (gpu-graph-study, "PageRank T4": <= 32, 33..1024,
-// > 1024; in-degree 0 gathers nothing), and the rows above 1024 are cut into
+//   4. k_scan_excl   in_ptr = exclusive prefix sum of the in-degrees, in one
+//                    pass with decoupled look-back between tiles
+//
+// Classes (gpu-graph-study, "PageRank T4": in-degree > 1024, 33..1024, 1..32,
+// and 0) give the class-major work order: one more stable counting-sort pass
+// over the vertices, keyed by class (CTA rows first, then warp, thread and
+// zero rows) and, inside a class, by half-octave bucket of the out-degree,
+// largest first (ties by id).
+//
+// Work layout. The iteration does not run on the in-edge CSR above (which is
+// kept, bit for bit, for pr_get_in_csr) but on the same graph relabelled by
+// that class-major order: vertex v becomes perm[v], row i of the work CSR
+// (w_ptr, w_col) is the in-row of order[i] with every source u replaced by
+// perm[u]. Each class is then a contiguous range of rows and of edges, the
+// per-row state is read and written in order, and, since the order leads with
+// in-degree hubs sorted by out-degree, the most gathered values of skewed
+// graphs sit together at the start of the state vector (where the iteration
+// keeps a copy in shared memory). Rows above 1024 in-edges are cut into
 // fixed-size edge chunks.
 //
-// Every wait in this file (the look-back) is bounded: after kSpinLimit polls
-// it sets kErrTimeout in the error word and moves on, so no launch can hang.
+// Every wait in this file (the look-backs) is bounded: after kSpinLimit polls
+// it sets kErrTimeout in the error word and moves on, the host stops the
+// build at the next check, and every store whose offset came out of a
+// look-back is range-checked, so no launch can hang or write out of bounds.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,7 +54,7 @@ namespace {
 constexpr unsigned long long kFlagA = 1ull << 62;   // tile aggregate published
 constexpr unsigned long long kFlagP = 2ull << 62;   // inclusive prefix published
 constexpr unsigned long long kValueMask = (1ull << 62) - 1;
-constexpr int kSpinLimit = 1 << 20;
+constexpr int kSpinLimit = 1 << 22;
 
 __device__ __forceinline__ unsigned long long load_desc(const unsigned long long *p)
 {
@@ -48,26 +68,25 @@ __device__ __forceinline__ void store_desc(unsigned long long *p, unsigned long 
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Waits (bounded) for a published descriptor; returns 0 on timeout.
+// Waits (bounded) for a published descriptor; returns 0 on timeout. Polls
+// back to back first (the predecessor is usually moments away), then backs off.
 __device__ __forceinline__ unsigned long long wait_desc(const unsigned long long *p, unsigned *err)
 {
     unsigned long long v = load_desc(p);
     int spins = 0;
-    unsigned ns = 32;
     while ((v >> 62) == 0) {
         if (++spins > kSpinLimit) {
             atomicOr(err, kErrTimeout);
             return 0;
         }
-        __nanosleep(ns);
-        if (ns < 1024)
-            ns <<= 1;
+        if (spins > 64)
+            __nanosleep(spins > 4096 ? 256 : 32);
         v = load_desc(p);
     }
     return v;
 }
 
-// Sum of everything published before `tile` for one descriptor column (walks
+// Sum of everything published before `tile` in one descriptor column (walks
 // back until an inclusive prefix is found). Tile 0 always publishes kFlagP.
 __device__ long long look_back(const unsigned long long *desc, int64_t tile, int64_t stride,
                                unsigned *err)
@@ -82,6 +101,74 @@ __device__ long long look_back(const unsigned long long *desc, int64_t tile, int
             break;
     }
     return prefix;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        T t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v += t;
+    }
+    return v;
+}
+
+// First index i in [0, len) with a[i] > key (len if none).
+template <typename I>
+__device__ __forceinline__ int64_t upper_bound(const I *a, int64_t len, int64_t key)
+{
+    int64_t lo = 0, hi = len;
+    while (lo < hi) {
+        int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)a[mid] <= key)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Advances row r (off[r] <= i) to the row holding offset i: galloping (1, 2,
+// 4, ... rows) then bisection, so runs of empty rows cost O(log gap).
+// `last` is the index of the final offset; requires off[last] > i, so no
+// index beyond `last` is read.
+template <typename I>
+__device__ __forceinline__ int64_t advance_row(const I *off, int64_t r, int64_t i, int64_t last)
+{
+    if ((int64_t)off[r + 1] > i)
+        return r;
+    int64_t lo = r + 1, step = 1;   // off[lo] <= i
+    int64_t hi = min(lo + step, last);
+    while ((int64_t)off[hi] <= i) {
+        lo = hi;
+        step <<= 1;
+        hi = min(lo + step, last);
+    }
+    while (hi - lo > 1) {   // off[lo] <= i < off[hi]
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)off[mid] <= i)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Row of offset i in a CSR offset array: the r with off[r] <= i < off[r+1],
+// searched in (lo, hi) where off[lo] <= i < off[hi].
+template <typename I>
+__device__ __forceinline__ int64_t row_of(const I *off, int64_t lo, int64_t hi, int64_t i)
+{
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)off[mid] <= i)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
 }
 
 // ---------------------------------------------------------------- step 1 --
@@ -111,67 +198,301 @@ __global__ void k_outdeg(int64_t n, const int64_t *__restrict__ row_ptr,
 
 // ---------------------------------------------------------------- step 2 --
 
-// First index i in [0, len) with a[i] > key (len if none).
-__device__ __forceinline__ int64_t upper_bound_i64(const int64_t *a, int64_t len, int64_t key)
+constexpr int kRadixBits = 8;
+constexpr int kRadixBins = 1 << kRadixBits;
+constexpr int kRadixItems = 8;
+constexpr int kRadixTile = kBlock * kRadixItems;
+constexpr int kMaxPasses = 4;
+
+// The digit counts of every pass, and (n > 0) a range check of every key
+// against [0, n).
+__global__ void __launch_bounds__(kBlock)
+k_digit_hist(const int32_t *__restrict__ keys, int64_t count, int64_t n, int passes,
+             unsigned *__restrict__ hist, unsigned *err)
 {
-    int64_t lo = 0, hi = len;
-    while (lo < hi) {
-        int64_t mid = (lo + hi) >> 1;
-        if (a[mid] <= key)
-            lo = mid + 1;
-        else
-            hi = mid;
+    __shared__ unsigned s_h[kMaxPasses][kRadixBins];
+    for (int i = threadIdx.x; i < kMaxPasses * kRadixBins; i += kBlock)
+        (&s_h[0][0])[i] = 0;
+    __syncthreads();
+    bool bad = false;
+    for (int64_t i = blockIdx.x * (int64_t)kBlock + threadIdx.x; i < count;
+         i += (int64_t)gridDim.x * kBlock) {
+        const int32_t v = keys[i];
+        if (n > 0 && (v < 0 || (int64_t)v >= n)) {
+            bad = true;
+            continue;
+        }
+        for (int p = 0; p < passes; ++p)
+            atomicAdd(&s_h[p][((unsigned)v >> (p * kRadixBits)) & (kRadixBins - 1)], 1u);
     }
-    return lo;
+    if (bad)
+        atomicOr(err, kErrColIdx);
+    __syncthreads();
+    for (int p = 0; p < passes; ++p) {
+        const unsigned c = s_h[p][threadIdx.x];
+        if (c)
+            atomicAdd(&hist[p * kRadixBins + threadIdx.x], c);
+    }
 }
 
-constexpr int kExpandItems = 8;
-
-// Source of every edge, range check of the targets and the in-degree
-// histogram. Requires row_ptr[0] == 0 and row_ptr[n] == m (checked on the
-// host before launch), which keeps every index below in range even when
-// row_ptr is not monotone (that case is flagged by k_outdeg and the build
-// stops before the sources are used).
-__global__ void __launch_bounds__(kBlock)
-k_expand(int64_t n, int64_t m, const int64_t *__restrict__ row_ptr,
-         const int32_t *__restrict__ col, int32_t *__restrict__ src,
-         int32_t *__restrict__ in_deg, unsigned *err)
+// Exclusive scan of each pass's 256 digit counts: where each digit's bucket starts.
+__global__ void __launch_bounds__(kRadixBins)
+k_digit_base(const unsigned *__restrict__ hist, int passes, unsigned *__restrict__ base)
 {
-    __shared__ int64_t s_lo, s_hi;
-    const int64_t tile = (int64_t)kBlock * kExpandItems;
-    for (int64_t j0 = blockIdx.x * tile; j0 < m; j0 += (int64_t)gridDim.x * tile) {
-        const int64_t j1 = min(j0 + tile, m);
-        if (threadIdx.x == 0) {
-            s_lo = upper_bound_i64(row_ptr, n + 1, j0) - 1;
-            s_hi = upper_bound_i64(row_ptr, n + 1, j1 - 1);
-        }
+    __shared__ unsigned s_w[kRadixBins / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int p = 0; p < passes; ++p) {
+        const unsigned c = hist[p * kRadixBins + threadIdx.x];
+        const unsigned incl = warp_incl_scan(c, lane);
+        if (lane == 31)
+            s_w[warp] = incl;
         __syncthreads();
-        const int64_t lo0 = s_lo, hi0 = s_hi;
-#pragma unroll
-        for (int k = 0; k < kExpandItems; ++k) {
-            const int64_t j = j0 + (int64_t)k * kBlock + threadIdx.x;
-            if (j < j1) {
-                int64_t lo = lo0, hi = hi0;   // row_ptr[lo] <= j < row_ptr[hi]
-                while (hi - lo > 1) {
-                    int64_t mid = (lo + hi) >> 1;
-                    if (row_ptr[mid] <= j)
-                        lo = mid;
-                    else
-                        hi = mid;
-                }
-                src[j] = (int32_t)lo;
-                const int32_t v = col[j];
-                if (v < 0 || (int64_t)v >= n)
-                    atomicOr(err, kErrColIdx);
-                else
-                    atomicAdd(&in_deg[v], 1);
-            }
-        }
+        unsigned off = 0;
+        for (int w = 0; w < warp; ++w)
+            off += s_w[w];
+        base[p * kRadixBins + threadIdx.x] = off + incl - c;
         __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------- step 3 --
+
+// One stable counting-sort pass over digit (key >> shift) & 255.
+//
+// Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
+// walks them in 32-key rounds, so "earlier round, then lower lane" is input
+// order. In each round __match_any_sync groups lanes with equal digits; a
+// per-warp shared counter carries each digit's running count across rounds.
+// Per-warp counts are then scanned across warps (and across digits for the
+// tile-local order), the tile is staged in shared memory in (digit, input)
+// order, and the prefix over earlier tiles comes from a per-digit look-back.
+// The write-out walks the staged tile linearly, so a warp stores consecutive
+// addresses of one bucket.
+//
+// kFlags:
+//   kSrcRows   the values are the edges' sources: the input is the out-edge
+//              CSR's col_idx, and position i belongs to the row r with
+//              row_ptr[r] <= i < row_ptr[r+1]. The tile marks the start of
+//              every row that begins inside it and takes a max-scan, so each
+//              position learns its row without a per-key search.
+//   kWriteKeys the keys are written too (not on the last pass).
+//   kHistogram the last pass of the edge sort: the tile, ordered by full key
+//              within each digit bucket, adds each run of equal keys to the
+//              in-degree histogram once.
+enum : unsigned { kSrcRows = 1u, kWriteKeys = 2u, kHistogram = 4u };
+
+__device__ __forceinline__ int spad(int i) { return i + (i >> 5); }   // bank-conflict padding
+
+// Block-wide inclusive max-scan of `count` shared entries, kRadixItems
+// consecutive entries per thread.
+__device__ __forceinline__ void block_max_scan(int32_t *a, int count, int32_t *s_wmax)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int j0 = tid * kRadixItems;
+    int32_t run = INT32_MIN;
+    for (int j = j0; j < j0 + kRadixItems && j < count; ++j)
+        run = max(run, a[spad(j)]);
+    int32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl = max(incl, t);
+    }
+    if (lane == 31)
+        s_wmax[warp] = incl;
+    __syncthreads();
+    int32_t carry = INT32_MIN;
+    for (int w = 0; w < warp; ++w)
+        carry = max(carry, s_wmax[w]);
+    const int32_t up = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane > 0)
+        carry = max(carry, up);
+    for (int j = j0; j < j0 + kRadixItems && j < count; ++j) {
+        carry = max(carry, a[spad(j)]);
+        a[spad(j)] = carry;
+    }
+    __syncthreads();
+}
+
+template <unsigned kFlags>
+__global__ void __launch_bounds__(kBlock, 4)
+k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ vals_in,
+             const int64_t *__restrict__ row_ptr, int64_t n, int32_t *__restrict__ keys_out,
+             int32_t *__restrict__ vals_out, int32_t *__restrict__ in_deg, int64_t count,
+             int shift, const unsigned *__restrict__ digit_base, unsigned long long *desc,
+             unsigned *tile_counter, unsigned *err)
+{
+    constexpr int kWarps = kBlock / 32;
+    constexpr int kWarpSpan = 32 * kRadixItems;
+    constexpr int kPadTile = kRadixTile + kRadixTile / 32;
+    __shared__ unsigned s_wh[kWarps][kRadixBins];   // per-warp counts, then offsets
+    __shared__ unsigned s_start[kRadixBins];        // tile-local start of each digit
+    __shared__ unsigned s_base[kRadixBins];         // global start of this tile's digit run
+    __shared__ unsigned s_wsum[kWarps];
+    __shared__ int32_t s_wmax[kWarps];
+    __shared__ int32_t s_key[kPadTile];
+    __shared__ int32_t s_val[kPadTile];             // also the row map of kSrcRows
+    __shared__ int64_t s_row_lo, s_row_hi;
+    __shared__ unsigned s_tile;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0)
+        s_tile = atomicAdd(tile_counter, 1u);
+    for (int w = 0; w < kWarps; ++w)
+        s_wh[w][tid] = 0;
+    __syncthreads();
+    const int64_t tile = s_tile;
+    const int64_t tile_begin = tile * kRadixTile;
+    const int tile_count = (int)min((int64_t)kRadixTile, count - tile_begin);
+    const int64_t base = tile_begin + (int64_t)warp * kWarpSpan;
+
+    if (kFlags & kSrcRows) {
+        // row of every position of the tile: mark row starts, then max-scan
+        if (tid == 0) {
+            s_row_lo = upper_bound(row_ptr, n + 1, tile_begin) - 1;
+            s_row_hi = upper_bound(row_ptr, n + 1, tile_begin + tile_count - 1) - 1;
+        }
+        for (int j = tid; j < tile_count; j += kBlock)
+            s_val[spad(j)] = INT32_MIN;
+        __syncthreads();
+        const int64_t rlo = s_row_lo, rhi = s_row_hi;
+        if (tid == 0)
+            s_val[spad(0)] = (int32_t)rlo;
+        __syncthreads();
+        for (int64_t r = rlo + 1 + tid; r <= rhi; r += kBlock) {
+            const int64_t p = row_ptr[r] - tile_begin;   // in [1, tile_count) for r in (rlo, rhi]
+            if (p > 0 && p < tile_count)
+                atomicMax(&s_val[spad((int)p)], (int32_t)r);
+        }
+        __syncthreads();
+        block_max_scan(s_val, tile_count, s_wmax);
+    }
+
+    int32_t key[kRadixItems], val[kRadixItems];
+    unsigned rank[kRadixItems];
+#pragma unroll
+    for (int r = 0; r < kRadixItems; ++r) {
+        const int64_t i = base + r * 32 + lane;
+        const bool ok = i < count;
+        key[r] = ok ? keys_in[i] : 0;
+        if (kFlags & kSrcRows)
+            val[r] = ok ? s_val[spad((int)(i - tile_begin))] : 0;
+        else
+            val[r] = ok ? vals_in[i] : 0;
+    }
+    if (kFlags & kSrcRows)
+        __syncthreads();   // s_val is reused for staging below
+
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < kRadixItems; ++r) {
+        const bool ok = base + r * 32 + lane < count;
+        const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
+        const unsigned peers = __match_any_sync(0xffffffffu, dig);
+        const unsigned before = ok ? s_wh[warp][dig] : 0u;
+        __syncwarp();
+        rank[r] = before + __popc(peers & below);
+        if (ok && (peers >> lane) == 1u)   // highest lane of the group
+            s_wh[warp][dig] = before + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // thread tid owns digit tid: exclusive offsets of the warps, the tile
+    // count, published at once so that later tiles can look back past us
+    unsigned tot = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        const unsigned c = s_wh[w][tid];
+        s_wh[w][tid] = tot;
+        tot += c;
+    }
+    unsigned long long *my = desc + tile * kRadixBins + tid;
+    store_desc(my, (tile == 0 ? kFlagP : kFlagA) | tot);
+
+    // tile-local start of each digit (exclusive scan over the 256 digits)
+    const unsigned incl = warp_incl_scan(tot, lane);
+    if (lane == 31)
+        s_wsum[warp] = incl;
+    __syncthreads();
+    unsigned woff = 0;
+    for (int w = 0; w < warp; ++w)
+        woff += s_wsum[w];
+    s_start[tid] = woff + incl - tot;
+    __syncthreads();
+
+    // stage the tile in (digit, input) order
+#pragma unroll
+    for (int r = 0; r < kRadixItems; ++r) {
+        if (base + r * 32 + lane < count) {
+            const unsigned dig = ((unsigned)key[r] >> shift) & (kRadixBins - 1);
+            const int lp = (int)(s_start[dig] + s_wh[warp][dig] + rank[r]);
+            s_key[spad(lp)] = key[r];
+            s_val[spad(lp)] = val[r];
+        }
+    }
+
+    // prefix over earlier tiles
+    long long prefix = 0;
+    if (tile > 0) {
+        prefix = look_back(desc + tid, tile, kRadixBins, err);
+        store_desc(my, kFlagP | (unsigned long long)(prefix + tot));
+    }
+    s_base[tid] = digit_base[tid] + (unsigned)prefix;
+    __syncthreads();
+
+    // write-out: consecutive staged entries of one digit go to consecutive addresses
+#pragma unroll
+    for (int k = 0; k < kRadixItems; ++k) {
+        const int i = k * kBlock + tid;
+        if (i < tile_count) {
+            const int32_t kv = s_key[spad(i)];
+            const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
+            const int64_t pos = (int64_t)s_base[dig] + (i - (int)s_start[dig]);
+            if (pos < 0 || pos >= count)   // only reachable after a look-back timeout
+                continue;
+            vals_out[pos] = s_val[spad(i)];
+            if (kFlags & kWriteKeys)
+                keys_out[pos] = kv;
+        }
+    }
+
+    if (kFlags & kHistogram) {
+        // thread t owns staged entries [t*ITEMS, (t+1)*ITEMS); each run of
+        // equal keys adds its length once, at its last entry. The head of
+        // the run an entry belongs to comes from a max-scan of run heads.
+        const int j0 = tid * kRadixItems;
+        int head_local = -1;
+        for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j)
+            if (j == 0 || s_key[spad(j)] != s_key[spad(j - 1)])
+                head_local = j;
+        int carry = head_local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, carry, o);
+            if (lane >= o)
+                carry = max(carry, t);
+        }
+        if (lane == 31)
+            s_wmax[warp] = carry;
+        __syncthreads();
+        int head = -1;
+        for (int w = 0; w < warp; ++w)
+            head = max(head, s_wmax[w]);
+        const int up = __shfl_up_sync(0xffffffffu, carry, 1);
+        if (lane > 0)
+            head = max(head, up);   // last run head before this thread's entries
+        for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j) {
+            const int32_t kv = s_key[spad(j)];
+            if (j == 0 || kv != s_key[spad(j - 1)])
+                head = j;
+            if ((j == tile_count - 1 || s_key[spad(j + 1)] != kv) && kv >= 0 && (int64_t)kv < n)
+                atomicAdd(&in_deg[kv], j - head + 1);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- step 4 --
 
 constexpr int kScanItems = 16;
 constexpr int kScanTile = kBlock * kScanItems;
@@ -181,28 +502,28 @@ struct LoadCount {   // element i of an int32 array
     __device__ int32_t operator()(int64_t i) const { return p[i]; }
 };
 
-__device__ __forceinline__ int row_class(int32_t deg)
+// Length of work row i: the in-degree of order[i], rounded up to a multiple
+// of 4 for CTA and warp rows so that their edges start 16-byte aligned.
+__device__ __forceinline__ int32_t padded_degree(int32_t deg)
 {
-    return deg == 0 ? kClassZero : deg <= kThreadMax ? kClassThread
-                                   : deg <= kWarpMax ? kClassWarp : kClassCta;
+    return deg > kThreadMax ? ((deg + 3) & ~3) : deg;
 }
 
-struct LoadClassFlag {   // 1 if row i is in class cls
+struct LoadOrderDeg {
     const int32_t *in_ptr;
-    int cls;
+    const int32_t *order;
     __device__ int32_t operator()(int64_t i) const
     {
-        return row_class(in_ptr[i + 1] - in_ptr[i]) == cls ? 1 : 0;
+        const int32_t v = order[i];
+        return padded_degree(in_ptr[v + 1] - in_ptr[v]);
     }
 };
 
-struct LoadChunkCount {   // number of edge chunks of CTA row i
-    const int32_t *in_ptr;
-    const int32_t *rows_c;
+struct LoadChunkCount {   // number of edge chunks of work row i
+    const int32_t *w_ptr;
     __device__ int32_t operator()(int64_t i) const
     {
-        const int32_t v = rows_c[i];
-        const int64_t deg = (int64_t)in_ptr[v + 1] - in_ptr[v];
+        const int64_t deg = (int64_t)w_ptr[i + 1] - w_ptr[i];
         return (int32_t)((deg + kChunkEdges - 1) / kChunkEdges);
     }
 };
@@ -215,7 +536,7 @@ __global__ void __launch_bounds__(kBlock)
 k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
             unsigned long long *desc, unsigned *tile_counter, unsigned *err)
 {
-    __shared__ int32_t s_items[kScanTile];
+    __shared__ int32_t s_items[kScanTile + kScanTile / 32];   // padded: no bank conflicts
     __shared__ long long s_warp[kBlock / 32];
     __shared__ long long s_prefix;
     __shared__ unsigned s_tile;
@@ -226,10 +547,11 @@ k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
     __syncthreads();
     const int64_t tile = s_tile;
     const int64_t base = tile * kScanTile;
+    auto pad = [](int i) { return i + (i >> 5); };
 
     for (int k = 0; k < kScanItems; ++k) {
         const int64_t i = base + (int64_t)k * kBlock + tid;
-        s_items[k * kBlock + tid] = (i < count) ? load(i) : 0;
+        s_items[pad(k * kBlock + tid)] = (i < count) ? load(i) : 0;
     }
     __syncthreads();
 
@@ -237,16 +559,10 @@ k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
     long long local = 0;
 #pragma unroll
     for (int k = 0; k < kScanItems; ++k) {
-        v[k] = s_items[tid * kScanItems + k];
+        v[k] = s_items[pad(tid * kScanItems + k)];
         local += v[k];
     }
-    // block-wide exclusive scan of the per-thread sums
-    long long incl = local;
-    for (int o = 1; o < 32; o <<= 1) {
-        long long t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += t;
-    }
+    const long long incl = warp_incl_scan(local, lane);
     if (lane == 31)
         s_warp[warp] = incl;
     __syncthreads();
@@ -275,172 +591,124 @@ k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
     long long run = s_prefix + thread_excl;
 #pragma unroll
     for (int k = 0; k < kScanItems; ++k) {
-        s_items[tid * kScanItems + k] = (int32_t)run;
+        s_items[pad(tid * kScanItems + k)] = (int32_t)run;
         run += v[k];
     }
     __syncthreads();
     for (int k = 0; k < kScanItems; ++k) {
         const int64_t i = base + (int64_t)k * kBlock + tid;
         if (i < count)
-            out[i] = s_items[k * kBlock + tid];
-    }
-}
-
-// ---------------------------------------------------------------- step 4 --
-
-constexpr int kRadixBits = 8;
-constexpr int kRadixBins = 1 << kRadixBits;
-constexpr int kRadixItems = 16;
-constexpr int kRadixTile = kBlock * kRadixItems;
-constexpr int kMaxPasses = 4;
-
-// Digit counts of every pass at once (one read of the keys).
-__global__ void __launch_bounds__(kBlock)
-k_digit_hist(const int32_t *__restrict__ keys, int64_t count, int passes,
-             unsigned *__restrict__ hist)
-{
-    __shared__ unsigned s_h[kMaxPasses][kRadixBins];
-    for (int i = threadIdx.x; i < kMaxPasses * kRadixBins; i += kBlock)
-        (&s_h[0][0])[i] = 0;
-    __syncthreads();
-    for (int64_t i = blockIdx.x * (int64_t)kBlock + threadIdx.x; i < count;
-         i += (int64_t)gridDim.x * kBlock) {
-        const unsigned k = (unsigned)keys[i];
-        for (int p = 0; p < passes; ++p)
-            atomicAdd(&s_h[p][(k >> (p * kRadixBits)) & (kRadixBins - 1)], 1u);
-    }
-    __syncthreads();
-    for (int p = 0; p < passes; ++p) {
-        const unsigned c = s_h[p][threadIdx.x];
-        if (c)
-            atomicAdd(&hist[p * kRadixBins + threadIdx.x], c);
-    }
-}
-
-// Exclusive scan of each pass's 256 digit counts: where each digit's bucket starts.
-__global__ void k_digit_base(const unsigned *__restrict__ hist, int passes,
-                             unsigned *__restrict__ base)
-{
-    __shared__ unsigned s[kRadixBins];
-    for (int p = 0; p < passes; ++p) {
-        s[threadIdx.x] = hist[p * kRadixBins + threadIdx.x];
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            unsigned run = 0;
-            for (int d = 0; d < kRadixBins; ++d) {
-                unsigned c = s[d];
-                s[d] = run;
-                run += c;
-            }
-        }
-        __syncthreads();
-        base[p * kRadixBins + threadIdx.x] = s[threadIdx.x];
-        __syncthreads();
-    }
-}
-
-// One stable counting-sort pass over digit (key >> shift) & 255.
-// Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
-// walks them in 32-key rounds, so "earlier round, then lower lane" is input
-// order. Within a warp, __match_any_sync groups equal digits of a round and a
-// per-warp shared counter carries the running count across rounds; per-warp
-// counts are then scanned across warps, and across tiles by look-back (one
-// thread per digit).
-template <bool kWriteKeys>
-__global__ void __launch_bounds__(kBlock)
-k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ vals_in,
-             int32_t *__restrict__ keys_out, int32_t *__restrict__ vals_out, int64_t count,
-             int shift, const unsigned *__restrict__ digit_base, unsigned long long *desc,
-             unsigned *tile_counter, unsigned *err)
-{
-    constexpr int kWarps = kBlock / 32;
-    constexpr int kWarpSpan = 32 * kRadixItems;
-    __shared__ unsigned s_wh[kWarps][kRadixBins];
-    __shared__ unsigned s_base[kRadixBins];
-    __shared__ unsigned s_tile;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        s_tile = atomicAdd(tile_counter, 1u);
-    for (int w = 0; w < kWarps; ++w)
-        s_wh[w][tid] = 0;
-    __syncthreads();
-    const int64_t tile = s_tile;
-    const int64_t base = tile * kRadixTile + (int64_t)warp * kWarpSpan;
-
-    int32_t key[kRadixItems], val[kRadixItems];
-    unsigned rank[kRadixItems], dig[kRadixItems];
-#pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
-        const int64_t i = base + r * 32 + lane;
-        const bool ok = i < count;
-        key[r] = ok ? keys_in[i] : 0;
-        val[r] = ok ? vals_in[i] : 0;
-        dig[r] = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
-    }
-    const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
-        const unsigned peers = __match_any_sync(0xffffffffu, dig[r]);
-        const bool ok = dig[r] < kRadixBins;
-        const unsigned before = ok ? s_wh[warp][dig[r]] : 0u;
-        __syncwarp();
-        rank[r] = before + __popc(peers & below);
-        if (ok && (peers >> lane) == 1u)   // highest lane of the group
-            s_wh[warp][dig[r]] = before + __popc(peers);
-        __syncwarp();
-    }
-    __syncthreads();
-
-    // thread tid owns digit tid: offsets of each warp, the tile's count, and
-    // the count of all earlier tiles
-    unsigned tot = 0;
-    for (int w = 0; w < kWarps; ++w) {
-        const unsigned c = s_wh[w][tid];
-        s_wh[w][tid] = tot;
-        tot += c;
-    }
-    long long prefix = 0;
-    unsigned long long *my = desc + tile * kRadixBins + tid;
-    if (tile == 0) {
-        store_desc(my, kFlagP | tot);
-    } else {
-        store_desc(my, kFlagA | tot);
-        prefix = look_back(desc + tid, tile, kRadixBins, err);
-        store_desc(my, kFlagP | (unsigned long long)(prefix + tot));
-    }
-    s_base[tid] = digit_base[tid] + (unsigned)prefix;
-    __syncthreads();
-
-#pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
-        if (dig[r] < kRadixBins) {
-            const unsigned pos = s_base[dig[r]] + s_wh[warp][dig[r]] + rank[r];
-            if ((int64_t)pos >= count)   // only reachable after a look-back timeout
-                continue;
-            vals_out[pos] = val[r];
-            if (kWriteKeys)
-                keys_out[pos] = key[r];
-        }
+            out[i] = s_items[pad(k * kBlock + tid)];
     }
 }
 
 // ------------------------------------------------------------ classes ---
 
-struct ClassLists {
-    const int32_t *pos[4];   // exclusive scans of the class flags
-    int32_t *rows[4];        // compacted row ids
-    int64_t count[4];        // list lengths
-};
+// Position of a class in the class-major order: CTA rows, warp rows, thread
+// rows, then rows without in-edges.
+__device__ __forceinline__ int class_slot(int32_t deg)
+{
+    return deg > kWarpMax ? 0 : deg > kThreadMax ? 1 : deg > 0 ? 2 : 3;
+}
 
-__global__ void k_compact(int64_t n, const int32_t *__restrict__ in_ptr, ClassLists L)
+// Half-octave bucket of an out-degree: 2*floor(log2(d+1)) plus the next bit.
+__device__ __forceinline__ int degree_bucket(int32_t deg)
+{
+    const unsigned x = (unsigned)deg + 1u;
+    const int b = 31 - __clz(x);
+    const int half = b > 0 ? (int)((x >> (b - 1)) & 1u) : 0;
+    return min(63, 2 * b + half);
+}
+
+// Sort key of the work order: class slot, then out-degree bucket, largest
+// first (the most gathered vertices lead), ties by vertex id (the sort is
+// stable over vals = ids).
+__global__ void k_order_keys(int64_t n, const int32_t *__restrict__ in_ptr,
+                             const int32_t *__restrict__ deg_out, int32_t *__restrict__ keys,
+                             int32_t *__restrict__ vals)
 {
     for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n;
          v += (int64_t)gridDim.x * blockDim.x) {
-        const int c = row_class(in_ptr[v + 1] - in_ptr[v]);
-        const int32_t p = L.pos[c][v];
-        if (p >= 0 && p < L.count[c])
-            L.rows[c][p] = (int32_t)v;
+        keys[v] = class_slot(in_ptr[v + 1] - in_ptr[v]) * 64 + (63 - degree_bucket(deg_out[v]));
+        vals[v] = (int32_t)v;
+    }
+}
+
+__global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *__restrict__ perm)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t v = order[i];
+        if (v >= 0 && (int64_t)v < n)
+            perm[v] = (int32_t)i;
+    }
+}
+
+// The work CSR: w_col[w_ptr[i] + k] = perm[in_col[in_ptr[order[i]] + k]] for
+// k below the in-degree, and n (the zero slot) in the padding. Edge-parallel:
+// each block writes one tile of w_col, finding each entry's work row with one
+// search and a forward walk.
+constexpr int kRelabelItems = 16;
+
+__global__ void __launch_bounds__(kBlock)
+k_relabel(int64_t n, int64_t m, const int32_t *__restrict__ w_ptr, const int32_t *__restrict__ order,
+          const int32_t *__restrict__ perm, const int32_t *__restrict__ in_ptr,
+          const int32_t *__restrict__ in_col, int32_t *__restrict__ w_col)
+{
+    __shared__ int64_t s_lo, s_hi;
+    const int64_t tile = (int64_t)kBlock * kRelabelItems;
+    for (int64_t j0 = blockIdx.x * tile; j0 < m; j0 += (int64_t)gridDim.x * tile) {
+        const int64_t j1 = min(j0 + tile, m);
+        if (threadIdx.x == 0) {
+            s_lo = upper_bound(w_ptr, n + 1, j0) - 1;
+            s_hi = upper_bound(w_ptr, n + 1, j1 - 1);
+        }
+        __syncthreads();
+        int64_t row = -1, src_base = 0, dst_base = 0, row_end = 0, deg = 0;
+        for (int k = 0; k < kRelabelItems; ++k) {
+            const int64_t j = j0 + (int64_t)k * kBlock + threadIdx.x;
+            if (j >= j1)
+                break;
+            if (row < 0 || j >= row_end) {
+                row = (row < 0) ? row_of(w_ptr, s_lo, s_hi, j) : advance_row(w_ptr, row, j, n);
+                const int32_t v = order[row];
+                dst_base = w_ptr[row];
+                row_end = w_ptr[row + 1];
+                src_base = in_ptr[v];
+                deg = in_ptr[v + 1] - src_base;
+            }
+            const int64_t k_in_row = j - dst_base;
+            w_col[j] = (k_in_row < deg) ? perm[in_col[src_base + k_in_row]] : (int32_t)n;
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void k_permute_deg(int64_t n, const int32_t *__restrict__ order,
+                              const int32_t *__restrict__ deg_out, int32_t *__restrict__ w_deg)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        w_deg[i] = deg_out[order[i]];
+}
+
+// True in-edges of the CTA, warp and thread classes (work ranges [0, a),
+// [a, b), [b, c)), for reporting.
+__global__ void k_class_edges(int64_t c_end, int64_t a, int64_t b, const int32_t *__restrict__ in_ptr,
+                              const int32_t *__restrict__ order, unsigned long long *out)
+{
+    unsigned long long s[3] = {0, 0, 0};
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < c_end;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t v = order[i];
+        s[i < a ? 0 : i < b ? 1 : 2] += (unsigned long long)(in_ptr[v + 1] - in_ptr[v]);
+    }
+    for (int q = 0; q < 3; ++q) {
+        unsigned long long t = s[q];
+        for (int o = 16; o > 0; o >>= 1)
+            t += __shfl_xor_sync(0xffffffffu, t, o);
+        if ((threadIdx.x & 31) == 0 && t)
+            atomicAdd(out + q, t);
     }
 }
 
@@ -451,22 +719,6 @@ __global__ void k_fill_chunks(int64_t n_c, int64_t n_chunks, const int32_t *__re
         for (int32_t c = chunk_first[r] + threadIdx.x; c < chunk_first[r + 1]; c += blockDim.x)
             if (c >= 0 && c < n_chunks)
                 chunk_row[c] = (int32_t)r;
-}
-
-// Edges per class (for reporting): sum of in-degrees over each list.
-__global__ void k_class_edges(const int32_t *__restrict__ in_ptr, const int32_t *__restrict__ rows,
-                              int64_t count, unsigned long long *out)
-{
-    unsigned long long s = 0;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int32_t v = rows[i];
-        s += (unsigned long long)(in_ptr[v + 1] - in_ptr[v]);
-    }
-    for (int o = 16; o > 0; o >>= 1)
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-    if ((threadIdx.x & 31) == 0 && s)
-        atomicAdd(out, s);
 }
 
 // ------------------------------------------------------------- host side --
@@ -532,6 +784,16 @@ pr_status read_err(pr_graph *g, cudaStream_t s, unsigned *out)
     return e == cudaSuccess ? PR_OK : cuda_status(e, "reading the error word");
 }
 
+template <unsigned kFlags>
+void launch_pass(int64_t tiles, cudaStream_t s, const int32_t *kin, const int32_t *vin,
+                 const int64_t *row_ptr, int64_t n, int32_t *kout, int32_t *vout, int32_t *in_deg,
+                 int64_t count, int shift, const unsigned *dbase, unsigned long long *desc,
+                 unsigned *counter, unsigned *err)
+{
+    k_radix_pass<kFlags><<<(unsigned)tiles, kBlock, 0, s>>>(
+        kin, vin, row_ptr, n, kout, vout, in_deg, count, shift, dbase, desc, counter, err);
+}
+
 }  // namespace
 
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, cudaStream_t s)
@@ -555,27 +817,40 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
             return cuda_status(e, what);             \
     } while (0)
 
-    // handle-owned buffers
+    // handle-owned buffers: the in-edge CSR and the work layout
     PRK_TRY(graph_alloc(g, (void **)&g->in_ptr, (size_t)(n + 1) * sizeof(int32_t)));
     PRK_TRY(graph_alloc(g, (void **)&g->in_col, (size_t)(m + 4) * sizeof(int32_t)));
     PRK_TRY(graph_alloc(g, (void **)&g->deg_out, (size_t)n * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->order, (size_t)n * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->perm, (size_t)n * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->w_ptr, (size_t)(n + 1) * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->w_deg, (size_t)n * sizeof(int32_t)));
+
+    int bits = 0;
+    while (bits < 31 && ((int64_t)1 << bits) < n)
+        ++bits;
+    int passes = (bits + kRadixBits - 1) / kRadixBits;
+    if (passes < 1)
+        passes = 1;
 
     // scratch
-    int32_t *src = nullptr, *in_deg = nullptr;
-    unsigned long long *counters = nullptr;   // [0] = dangling, [1..3] = class edges
+    int32_t *in_deg = nullptr;
+    unsigned long long *counters = nullptr;   // [0] = dangling
     unsigned *tile_counter = nullptr, *hist = nullptr, *dbase = nullptr;
     unsigned long long *desc = nullptr;
-    PRK_TRY(tmp.alloc((void **)&src, (size_t)m * sizeof(int32_t)));
     PRK_TRY(tmp.alloc((void **)&in_deg, (size_t)n * sizeof(int32_t)));
     PRK_TRY(tmp.alloc((void **)&counters, 8 * sizeof(unsigned long long)));
     PRK_TRY(tmp.alloc((void **)&tile_counter, sizeof(unsigned)));
     PRK_TRY(tmp.alloc((void **)&hist, 2 * kMaxPasses * kRadixBins * sizeof(unsigned)));
     dbase = hist + kMaxPasses * kRadixBins;
-
     const int64_t scan_tiles = (n + 1 + kScanTile - 1) / kScanTile;
     const int64_t radix_tiles = (m + kRadixTile - 1) / kRadixTile;
-    const int64_t desc_words = scan_tiles > radix_tiles * kRadixBins ? scan_tiles
-                                                                     : radix_tiles * kRadixBins;
+    const int64_t order_tiles = (n + kRadixTile - 1) / kRadixTile;
+    int64_t desc_words = scan_tiles;
+    if (radix_tiles * kRadixBins > desc_words)
+        desc_words = radix_tiles * kRadixBins;
+    if (order_tiles * kRadixBins > desc_words)
+        desc_words = order_tiles * kRadixBins;
     PRK_TRY(tmp.alloc((void **)&desc, (size_t)(desc_words + 1) * sizeof(unsigned long long)));
 
     PRK_CUDA(cudaMemsetAsync(g->err, 0, sizeof(unsigned), s), "memset");
@@ -583,13 +858,13 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     PRK_CUDA(cudaMemsetAsync(counters, 0, 8 * sizeof(unsigned long long), s), "memset");
     PRK_CUDA(cudaMemsetAsync(hist, 0, kMaxPasses * kRadixBins * sizeof(unsigned), s), "memset");
 
-    // 1 + 2: degrees, sources, validation, in-degree histogram
+    // 1 + 2: degrees, validation, digit counts
     k_outdeg<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, d_row_ptr, g->deg_out, counters, g->err);
     ++g->build_launches;
-    if (m > 0)
-        k_expand<<<grid_for(m, kBlock * kExpandItems, cap), kBlock, 0, s>>>(
-            n, m, d_row_ptr, d_col, src, in_deg, g->err);
-    g->build_launches += (m > 0);
+    if (m > 0) {
+        k_digit_hist<<<grid_for(m, kBlock * 16, cap), kBlock, 0, s>>>(d_col, m, n, passes, hist, g->err);
+        ++g->build_launches;
+    }
     PRK_CUDA(cudaGetLastError(), "validation launch");
     unsigned herr = 0;
     PRK_TRY(read_err(g, s, &herr));
@@ -609,87 +884,106 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         return PR_OK;
     };
 
-    // 3: in_ptr = exclusive scan of the in-degrees (n + 1 outputs)
-    PRK_TRY(launch_scan(LoadCount{in_deg}, g->in_ptr, n, desc, tile_counter, g->err, &g->build_launches, s));
-
-    // 4: stable scatter by destination (LSD radix over 8-bit digits)
-    int bits = 0;
-    while (bits < 31 && ((int64_t)1 << bits) < n)
-        ++bits;
-    const int passes = (bits + kRadixBits - 1) / kRadixBits;
-    if (m > 0 && passes == 0) {
-        PRK_CUDA(cudaMemcpyAsync(g->in_col, src, (size_t)m * sizeof(int32_t),
-                                 cudaMemcpyDeviceToDevice, s), "copy");
-    } else if (m > 0) {
+    // 3: stable scatter by destination (LSD radix over 8-bit digits), which
+    // also yields the in-degree histogram
+    if (m > 0) {
         int32_t *kb[2] = {nullptr, nullptr}, *vb[2] = {nullptr, nullptr};
         for (int i = 0; i < 2 && i < passes - 1; ++i) {
             PRK_TRY(tmp.alloc((void **)&kb[i], (size_t)m * sizeof(int32_t)));
             PRK_TRY(tmp.alloc((void **)&vb[i], (size_t)m * sizeof(int32_t)));
         }
-        k_digit_hist<<<grid_for(m, kBlock * 16, cap), kBlock, 0, s>>>(d_col, m, passes, hist);
         k_digit_base<<<1, kRadixBins, 0, s>>>(hist, passes, dbase);
-        g->build_launches += 2;
-        PRK_CUDA(cudaGetLastError(), "digit histogram launch");
+        ++g->build_launches;
+        PRK_CUDA(cudaGetLastError(), "k_digit_base launch");
         for (int p = 0; p < passes; ++p) {
             const int32_t *kin = p == 0 ? d_col : kb[(p - 1) & 1];
-            const int32_t *vin = p == 0 ? src : vb[(p - 1) & 1];
-            const bool last = p == passes - 1;
+            const int32_t *vin = p == 0 ? nullptr : vb[(p - 1) & 1];
+            const bool first = p == 0, last = p == passes - 1;
             int32_t *vout = last ? g->in_col : vb[p & 1];
             int32_t *kout = last ? nullptr : kb[p & 1];
             PRK_CUDA(cudaMemsetAsync(desc, 0, (size_t)radix_tiles * kRadixBins * sizeof(unsigned long long), s),
                      "memset");
             PRK_CUDA(cudaMemsetAsync(tile_counter, 0, sizeof(unsigned), s), "memset");
-            if (last)
-                k_radix_pass<false><<<(unsigned)radix_tiles, kBlock, 0, s>>>(
-                    kin, vin, kout, vout, m, p * kRadixBits, dbase + p * kRadixBins, desc,
-                    tile_counter, g->err);
+            const int shift = p * kRadixBits;
+            const unsigned *db = dbase + p * kRadixBins;
+            if (first && last)
+                launch_pass<kSrcRows | kHistogram>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout,
+                                                   in_deg, m, shift, db, desc, tile_counter, g->err);
+            else if (first)
+                launch_pass<kSrcRows | kWriteKeys>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout,
+                                                   in_deg, m, shift, db, desc, tile_counter, g->err);
+            else if (last)
+                launch_pass<kHistogram>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
+                                        shift, db, desc, tile_counter, g->err);
             else
-                k_radix_pass<true><<<(unsigned)radix_tiles, kBlock, 0, s>>>(
-                    kin, vin, kout, vout, m, p * kRadixBits, dbase + p * kRadixBins, desc,
-                    tile_counter, g->err);
+                launch_pass<kWriteKeys>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
+                                        shift, db, desc, tile_counter, g->err);
             PRK_CUDA(cudaGetLastError(), "k_radix_pass launch");
             ++g->build_launches;
         }
     }
 
+    // 4: in_ptr = exclusive scan of the in-degrees (n + 1 outputs)
+    PRK_TRY(check_timeout());
+    PRK_TRY(launch_scan(LoadCount{in_deg}, g->in_ptr, n, desc, tile_counter, g->err,
+                        &g->build_launches, s));
     PRK_TRY(check_timeout());
 
-    // classes: flags -> exclusive scans -> compaction
-    int32_t *pos[4];
-    for (int c = 0; c < 4; ++c) {
-        PRK_TRY(tmp.alloc((void **)&pos[c], (size_t)(n + 1) * sizeof(int32_t)));
-        PRK_TRY(launch_scan(LoadClassFlag{g->in_ptr, c}, pos[c], n, desc, tile_counter, g->err, &g->build_launches, s));
+    // the work order: a stable counting sort of the vertices by (class,
+    // out-degree bucket), and its inverse
+    {
+        int32_t *okeys = nullptr, *ovals = nullptr;
+        PRK_TRY(tmp.alloc((void **)&okeys, (size_t)n * sizeof(int32_t)));
+        PRK_TRY(tmp.alloc((void **)&ovals, (size_t)n * sizeof(int32_t)));
+        PRK_CUDA(cudaMemsetAsync(hist, 0, kMaxPasses * kRadixBins * sizeof(unsigned), s), "memset");
+        k_order_keys<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, g->deg_out, okeys, ovals);
+        k_digit_hist<<<grid_for(n, kBlock * 16, cap), kBlock, 0, s>>>(okeys, n, 0, 1, hist, g->err);
+        k_digit_base<<<1, kRadixBins, 0, s>>>(hist, 1, dbase);
+        const int64_t otiles = (n + kRadixTile - 1) / kRadixTile;
+        PRK_CUDA(cudaMemsetAsync(desc, 0, (size_t)otiles * kRadixBins * sizeof(unsigned long long), s),
+                 "memset");
+        PRK_CUDA(cudaMemsetAsync(tile_counter, 0, sizeof(unsigned), s), "memset");
+        launch_pass<0u>(otiles, s, okeys, ovals, nullptr, n, nullptr, g->order, nullptr, n, 0, dbase,
+                        desc, tile_counter, g->err);
+        k_invert<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->perm);
+        g->build_launches += 5;
+        PRK_CUDA(cudaGetLastError(), "order launch");
     }
-    int32_t h_cnt[4];
-    for (int c = 0; c < 4; ++c)
-        PRK_CUDA(cudaMemcpyAsync(&h_cnt[c], pos[c] + n, sizeof(int32_t), cudaMemcpyDeviceToHost, s),
-                 "class counts");
+    unsigned h_hist[kRadixBins];
+    PRK_CUDA(cudaMemcpyAsync(h_hist, hist, sizeof(h_hist), cudaMemcpyDeviceToHost, s), "class counts");
     PRK_TRY(check_timeout());
-    g->n_z = h_cnt[0];
-    g->n_t = h_cnt[1];
-    g->n_w = h_cnt[2];
-    g->n_c = h_cnt[3];
-    PRK_TRY(graph_alloc(g, (void **)&g->rows_z, (size_t)g->n_z * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->rows_t, (size_t)g->n_t * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->rows_w, (size_t)g->n_w * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->rows_c, (size_t)g->n_c * sizeof(int32_t)));
+    int64_t cls[4] = {0, 0, 0, 0};
+    for (int b = 0; b < kRadixBins; ++b)
+        cls[b / 64] += h_hist[b];
+    g->n_c = cls[0];
+    g->n_w = cls[1];
+    g->n_t = cls[2];
+    g->n_z = cls[3];
+
+    // the work CSR in class-major order
+    PRK_TRY(launch_scan(LoadOrderDeg{g->in_ptr, g->order}, g->w_ptr, n, desc, tile_counter, g->err,
+                        &g->build_launches, s));
+    k_permute_deg<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->deg_out, g->w_deg);
+    ++g->build_launches;
+    int32_t h_mw = 0;
+    PRK_CUDA(cudaMemcpyAsync(&h_mw, g->w_ptr + n, sizeof(int32_t), cudaMemcpyDeviceToHost, s),
+             "work size");
+    PRK_TRY(check_timeout());
+    g->m_w = h_mw;
+    PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t)));
+    if (g->m_w > 0) {
+        k_relabel<<<grid_for(g->m_w, kBlock * kRelabelItems, cap), kBlock, 0, s>>>(
+            n, g->m_w, g->w_ptr, g->order, g->perm, g->in_ptr, g->in_col, g->w_col);
+        ++g->build_launches;
+    }
+    PRK_CUDA(cudaGetLastError(), "relabel launch");
+
+    // CTA rows (work rows [0, n_c)) -> chunks
     PRK_TRY(graph_alloc(g, (void **)&g->chunk_first, (size_t)(g->n_c + 1) * sizeof(int32_t)));
     PRK_TRY(graph_alloc(g, (void **)&g->hub_arrivals, (size_t)(g->n_c + 1) * sizeof(uint32_t)));
     PRK_CUDA(cudaMemsetAsync(g->hub_arrivals, 0, (size_t)(g->n_c + 1) * sizeof(uint32_t), s), "memset");
-    ClassLists lists;
-    int32_t *rows[4] = {g->rows_z, g->rows_t, g->rows_w, g->rows_c};
-    for (int c = 0; c < 4; ++c) {
-        lists.pos[c] = pos[c];
-        lists.rows[c] = rows[c];
-        lists.count[c] = h_cnt[c];
-    }
-    k_compact<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, lists);
-    ++g->build_launches;
-    PRK_CUDA(cudaGetLastError(), "k_compact launch");
-
-    // CTA rows -> chunks
-    PRK_TRY(launch_scan(LoadChunkCount{g->in_ptr, g->rows_c}, g->chunk_first, g->n_c, desc,
-                        tile_counter, g->err, &g->build_launches, s));
+    PRK_TRY(launch_scan(LoadChunkCount{g->w_ptr}, g->chunk_first, g->n_c, desc, tile_counter, g->err,
+                        &g->build_launches, s));
     int32_t h_chunks = 0;
     PRK_CUDA(cudaMemcpyAsync(&h_chunks, g->chunk_first + g->n_c, sizeof(int32_t),
                              cudaMemcpyDeviceToHost, s), "chunk count");
@@ -700,26 +994,23 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     if (g->n_c > 0)
         k_fill_chunks<<<grid_for(g->n_c, 1, cap), kBlock, 0, s>>>(g->n_c, g->n_chunks, g->chunk_first,
                                                                    g->chunk_row);
+    PRK_CUDA(cudaGetLastError(), "chunk launch");
 
-    // class edge counts (reporting only)
-    g->build_launches += (g->n_t > 0) + (g->n_w > 0) + (g->n_c > 0);
-    if (g->n_t)
-        k_class_edges<<<grid_for(g->n_t, kBlock, cap), kBlock, 0, s>>>(g->in_ptr, g->rows_t, g->n_t, counters + 1);
-    if (g->n_w)
-        k_class_edges<<<grid_for(g->n_w, kBlock, cap), kBlock, 0, s>>>(g->in_ptr, g->rows_w, g->n_w, counters + 2);
-    if (g->n_c)
-        k_class_edges<<<grid_for(g->n_c, kBlock, cap), kBlock, 0, s>>>(g->in_ptr, g->rows_c, g->n_c, counters + 3);
-    PRK_CUDA(cudaGetLastError(), "class launch");
-    unsigned long long h_counters[4];
+    // sizes for reporting: true in-edges per class, dangling count
+    const int64_t c_end = g->n_c + g->n_w + g->n_t;
+    if (c_end > 0) {
+        k_class_edges<<<grid_for(c_end, kBlock, cap), kBlock, 0, s>>>(
+            c_end, g->n_c, g->n_c + g->n_w, g->in_ptr, g->order, counters + 1);
+        ++g->build_launches;
+    }
+    unsigned long long h_counters[4] = {0, 0, 0, 0};
     PRK_CUDA(cudaMemcpyAsync(h_counters, counters, sizeof(h_counters), cudaMemcpyDeviceToHost, s),
              "counters");
-    PRK_TRY(read_err(g, s, &herr));
-    if (herr & kErrTimeout)
-        return set_error(PR_ERR_TIMEOUT, "a look-back wait in the transpose gave up");
+    PRK_TRY(check_timeout());
     g->n_dangling = (int64_t)h_counters[0];
-    g->e_t = (int64_t)h_counters[1];
+    g->e_c = (int64_t)h_counters[1];
     g->e_w = (int64_t)h_counters[2];
-    g->e_c = (int64_t)h_counters[3];
+    g->e_t = (int64_t)h_counters[3];
     return PR_OK;
 #undef PRK_TRY
 #undef PRK_CUDA
