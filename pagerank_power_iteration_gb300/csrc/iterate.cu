@@ -44,7 +44,7 @@ namespace {
 template <typename T>
 struct IterArgs {
     const int32_t *w_ptr;     // work CSR offsets (class-major order)
-    const int32_t *w_col;     // work sources; padding entries point at slot n
+    const int32_t *w_col;     // work sources; padding entries are kPadSource
     const int32_t *w_deg;     // out-degrees in work order
     const int32_t *chunk_row, *chunk_first;
     uint32_t *hub_arrivals;
@@ -55,11 +55,11 @@ struct IterArgs {
     const int32_t *perm;      // vertex id -> work position (start vector, output)
     const int32_t *order;     // work position -> vertex id
     const int32_t *deg_out;   // out-degrees by vertex id
+    const int32_t *w_split;   // [warps + 1]: warp-class rows of each warp of the grid
     int64_t n, n_c, n_w, n_t, n_z, n_chunks;
 };
 
 // streaming (evict-first) loads of the index stream
-__device__ __forceinline__ int32_t ld_stream(const int32_t *p) { return __ldcs(p); }
 __device__ __forceinline__ int4 ld_stream4(const int4 *p) { return __ldcs(p); }
 
 template <typename T>
@@ -88,7 +88,8 @@ __device__ __forceinline__ T block_sum(T v, T *red)
 }
 
 // The gathered state: slots below `hot` come from the CTA's shared-memory
-// copy of the head of the state vector, the rest from global memory.
+// copy of the head of the state vector, the rest from global memory, and a
+// padding entry (kPadSource, negative) contributes 0.
 template <typename T>
 struct Gather {
     const T *__restrict__ s;   // global state (s_old)
@@ -96,7 +97,7 @@ struct Gather {
     int32_t hot;
     __device__ __forceinline__ T operator()(int32_t u) const
     {
-        return u < hot ? h[u] : __ldg(s + u);
+        return u < 0 ? T(0) : u < hot ? h[u] : __ldg(s + u);
     }
     __device__ __forceinline__ T four(int4 q) const
     {
@@ -159,66 +160,87 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     T l1 = T(0), dm = T(0);
 
     // CTA class: rows with more than 1024 in-edges, cut into chunks of
-    // kChunkEdges (16-byte aligned, whole int4s). A CTA's warps take
-    // consecutive chunks, so a CTA streams kChunkEdges * 8 consecutive edges
-    // of a hub, but every warp reduces and hands off its own chunk: no
-    // CTA-wide barrier. The warp that finishes a row's last chunk adds the
-    // row's chunk partials in chunk order and combines the row.
+    // kChunkEdges (whole int4s). Warp gw streams the contiguous chunk range
+    // [gw * per, (gw + 1) * per), so a CTA streams 32 consecutive ranges of
+    // the hub edges. A warp sums each row's chunks in its range in registers;
+    // a row that lies wholly in the range is combined at once. A row that
+    // crosses a range boundary is handed off: each warp stores its piece's
+    // sum at the piece's first chunk (the row's first chunk, or a multiple of
+    // `per`), adds its chunk count to the row's arrival counter, and the warp
+    // that completes the count adds the pieces in chunk order and combines
+    // the row. No CTA-wide barrier, and no wait.
+    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
     {
         const int64_t nwarps = G * kWarps;
+        const int64_t per = (a.n_chunks + nwarps - 1) / nwarps;
+        const int64_t c_end = min((gw + 1) * per, a.n_chunks);
         const int4 *cv_all = reinterpret_cast<const int4 *>(a.w_col);
         constexpr int kVecPerLane = kChunkEdges / 4 / 32;
-        for (int64_t c = (int64_t)blockIdx.x * kWarps + warp; c < a.n_chunks; c += nwarps) {
+        int64_t c = gw * per;
+        while (c < c_end) {
             const int32_t r = a.chunk_row[c];
             const int32_t first = a.chunk_first[r];
             const int32_t nch = a.chunk_first[r + 1] - first;
-            const int64_t cb = a.w_ptr[r] + (int64_t)(c - first) * kChunkEdges;
-            const int64_t ce = min(cb + (int64_t)kChunkEdges, (int64_t)a.w_ptr[r + 1]);
-            const int nv = (int)((ce - cb) >> 2);
-            const int4 *cv = cv_all + (cb >> 2);
-            int4 q[kVecPerLane];
+            const int64_t stop = min((int64_t)first + nch, c_end);
+            const int64_t row_b = a.w_ptr[r], row_e = a.w_ptr[r + 1];
+            T acc = T(0);
+            for (int64_t cc = c; cc < stop; ++cc) {
+                const int64_t cb = row_b + (cc - first) * kChunkEdges;
+                const int nv = (int)((min(cb + (int64_t)kChunkEdges, row_e) - cb) >> 2);
+                const int4 *cv = cv_all + (cb >> 2);
+                int4 q[kVecPerLane];
 #pragma unroll
-            for (int t = 0; t < kVecPerLane; ++t)
-                if (lane + 32 * t < nv)
-                    q[t] = ld_stream4(cv + lane + 32 * t);
-            T part = T(0);
+                for (int t = 0; t < kVecPerLane; ++t)
+                    if (lane + 32 * t < nv)
+                        q[t] = ld_stream4(cv + lane + 32 * t);
 #pragma unroll
-            for (int t = 0; t < kVecPerLane; ++t)
-                if (lane + 32 * t < nv)
-                    part += gat.four(q[t]);
-            part = warp_sum(part);
-            uint32_t prev = 0;
-            if (lane == 0) {
-                __stcg(a.hub_partial + c, part);
-                __threadfence();
-                prev = atomicAdd(a.hub_arrivals + r, 1u);
+                for (int t = 0; t < kVecPerLane; ++t)
+                    if (lane + 32 * t < nv)
+                        acc += gat.four(q[t]);
             }
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev == (uint32_t)(nch - 1)) {
-                __threadfence();
-                T y = T(0);
-                for (int32_t k = lane; k < nch; k += 32)
-                    y += __ldcg(a.hub_partial + first + k);
-                y = warp_sum(y);
+            acc = warp_sum(acc);
+            const int32_t covered = (int32_t)(stop - c);
+            if (covered == nch) {
+                if (lane == 0)
+                    finish_row(r, acc, a.w_deg, s_old, s_new, base, d, l1, dm);
+            } else {
+                uint32_t prev = 0;
                 if (lane == 0) {
-                    a.hub_arrivals[r] = 0u;
-                    finish_row(r, y, a.w_deg, s_old, s_new, base, d, l1, dm);
+                    __stcg(a.hub_partial + c, acc);
+                    __threadfence();
+                    prev = atomicAdd(a.hub_arrivals + r, (uint32_t)covered);
+                }
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev + (uint32_t)covered == (uint32_t)nch) {
+                    __threadfence();
+                    T y = T(0);
+                    for (int32_t k = lane; k < nch; k += 32) {
+                        const int64_t cc = (int64_t)first + k;
+                        if (k == 0 || cc % per == 0)
+                            y += __ldcg(a.hub_partial + cc);
+                    }
+                    y = warp_sum(y);
+                    if (lane == 0) {
+                        a.hub_arrivals[r] = 0u;
+                        finish_row(r, y, a.w_deg, s_old, s_new, base, d, l1, dm);
+                    }
                 }
             }
+            c = stop;
         }
     }
 
     // warp class: one warp per row, 33..1024 in-edges (16-byte aligned,
-    // whole int4s). A warp takes 32 consecutive rows, reads their offsets in
-    // one coalesced load, walks them four rows at a time so that each lane
-    // has up to 16 gathers in flight, and finally combines row q in lane q.
+    // whole int4s). Each warp owns one contiguous range of these rows, cut so
+    // that every warp has about the same edges (w_split). It reads the
+    // offsets of 32 rows in one coalesced load, walks them four rows at a time
+    // so that each lane has up to 16 gathers in flight, and combines row q in
+    // lane q.
     {
-        const int64_t w0 = a.n_c, w1 = a.n_c + a.n_w;
-        const int64_t batches = (a.n_w + 31) / 32;
+        const int64_t r_begin = a.w_split[gw], r_end = a.w_split[gw + 1];
         const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
-        for (int64_t bi = (int64_t)blockIdx.x * kWarps + warp; bi < batches; bi += G * kWarps) {
-            const int64_t r0 = w0 + bi * 32;
-            const int cnt = (int)min((int64_t)32, w1 - r0);
+        for (int64_t r0 = r_begin; r0 < r_end; r0 += 32) {
+            const int cnt = (int)min((int64_t)32, r_end - r0);
             int32_t rb = 0, re = 0;
             if (lane < cnt) {
                 rb = a.w_ptr[r0 + lane];
@@ -260,32 +282,55 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         }
     }
 
-    // thread class: one thread per row, 1..32 in-edges; each thread walks two
-    // rows at once, two edges of each per step (missing edges gather the zero
-    // slot n), so four independent gathers are in flight
+    // thread class: one thread per row, 1..32 in-edges, padded to whole
+    // int4s. The warps of the grid sweep these rows together in blocks of 32;
+    // lane j owns row j of a block. The block's rows are contiguous in the
+    // work CSR, so the warp streams their int4s with coalesced loads (32 per
+    // step), finds the row of each int4 by bisection over the lanes' row
+    // starts, and forms the row sums with a segmented scan: the lane holding a
+    // row's last int4 of the step hands the run's sum to the row's owner. An
+    // int4 never straddles two rows (every row is padded), and every sum is
+    // formed in a fixed order.
     {
-        const int64_t t0 = a.n_c + a.n_w, t1 = t0 + a.n_t, stride = G * kIterBlock;
-        const int32_t zero_slot = (int32_t)a.n;
-        for (int64_t i = t0 + (int64_t)blockIdx.x * kIterBlock + tid; i < t1; i += 2 * stride) {
-            const int64_t i2 = i + stride;
-            const bool two = i2 < t1;
-            const int32_t b0 = a.w_ptr[i], e0 = a.w_ptr[i + 1];
-            const int32_t b1 = two ? a.w_ptr[i2] : 0, e1 = two ? a.w_ptr[i2 + 1] : 0;
-            T y0 = T(0), y1 = T(0), y2 = T(0), y3 = T(0);
-            const int32_t steps = max(e0 - b0, e1 - b1);
-            for (int32_t k = 0; k < steps; k += 2) {
-                const int32_t u0 = (b0 + k < e0) ? ld_stream(a.w_col + b0 + k) : zero_slot;
-                const int32_t u1 = (b0 + k + 1 < e0) ? ld_stream(a.w_col + b0 + k + 1) : zero_slot;
-                const int32_t u2 = (b1 + k < e1) ? ld_stream(a.w_col + b1 + k) : zero_slot;
-                const int32_t u3 = (b1 + k + 1 < e1) ? ld_stream(a.w_col + b1 + k + 1) : zero_slot;
-                y0 += gat(u0);
-                y1 += gat(u1);
-                y2 += gat(u2);
-                y3 += gat(u3);
+        const int64_t t_begin = a.n_c + a.n_w, t_end = t_begin + a.n_t;
+        const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
+        for (int64_t r0 = t_begin + gw * 32; r0 < t_end; r0 += G * kWarps * 32) {
+            const int cnt = (int)min((int64_t)32, t_end - r0);
+            const int32_t seg0 = a.w_ptr[r0] >> 2;
+            const int32_t nvec = (a.w_ptr[r0 + cnt] >> 2) - seg0;
+            // int4 range [cs, ce) of row `lane`, relative to the segment start
+            const int32_t cs = (lane < cnt) ? (a.w_ptr[r0 + lane] >> 2) - seg0 : nvec;
+            int32_t ce = __shfl_down_sync(0xffffffffu, cs, 1);
+            if (lane >= cnt - 1)
+                ce = nvec;
+            T acc = T(0);
+            for (int32_t p0 = 0; p0 < nvec; p0 += 32) {
+                const int32_t p = p0 + lane;
+                T v = T(0);
+                if (p < nvec)
+                    v = gat.four(ld_stream4(cv + seg0 + p));
+                int32_t row = 0;   // largest j < cnt with cs_j <= p
+#pragma unroll
+                for (int step = 16; step >= 1; step >>= 1) {
+                    const int32_t cand = row + step;
+                    const int32_t c_cs = __shfl_sync(0xffffffffu, cs, cand & 31);
+                    if (cand < cnt && c_cs <= p)
+                        row = cand;
+                }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const T t = __shfl_up_sync(0xffffffffu, v, o);
+                    const int32_t rr = __shfl_up_sync(0xffffffffu, row, o);
+                    if (lane >= o && rr == row)
+                        v += t;
+                }
+                const int32_t last = min(ce, p0 + 32) - 1;   // row's last int4 in this step
+                const T got = __shfl_sync(0xffffffffu, v, (last - p0) & 31);
+                if (lane < cnt && last >= max(cs, p0))
+                    acc += got;
             }
-            finish_row(i, y0 + y1, a.w_deg, s_old, s_new, base, d, l1, dm);
-            if (two)
-                finish_row(i2, y2 + y3, a.w_deg, s_old, s_new, base, d, l1, dm);
+            if (lane < cnt)
+                finish_row(r0 + lane, acc, a.w_deg, s_old, s_new, base, d, l1, dm);
         }
     }
 
@@ -349,7 +394,7 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
     const T x_uniform = T(1.0 / (double)a.n);
     T dm = T(0);
     if (blockIdx.x == 0 && tid == 0) {
-        a.s0[a.n] = T(0);   // the zero slot gathered by padding entries
+        a.s0[a.n] = T(0);   // slot n stays 0 (the shared copy may include it)
         a.s1[a.n] = T(0);
     }
     for (int64_t i = (int64_t)blockIdx.x * kBlock + tid; i < a.n; i += G * kBlock) {
@@ -406,6 +451,30 @@ __global__ void k_output(IterArgs<T> a, T *__restrict__ out)
     }
 }
 
+// Cuts rows [lo, hi) into `parts` contiguous ranges of about equal cost,
+// cost(i) = edges of rows lo..i-1 + row_cost * (i - lo): split[p] is the first
+// row whose cost reaches p/parts of the total (split[0] = lo, split[parts] = hi).
+__global__ void k_split(const int32_t *__restrict__ w_ptr, int64_t lo, int64_t hi, int64_t parts,
+                        int64_t row_cost, int32_t *__restrict__ split)
+{
+    const int64_t base_e = w_ptr[lo];
+    const double total = (double)(w_ptr[hi] - base_e) + (double)row_cost * (double)(hi - lo);
+    for (int64_t p = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; p <= parts;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const double target = total * (double)p / (double)parts;
+        int64_t a = lo, b = hi;   // first i in [lo, hi] with cost(i) >= target
+        while (a < b) {
+            const int64_t mid = (a + b) >> 1;
+            const double c = (double)(w_ptr[mid] - base_e) + (double)row_cost * (double)(mid - lo);
+            if (c >= target)
+                b = mid;
+            else
+                a = mid + 1;
+        }
+        split[p] = (int32_t)(p == parts ? hi : a);
+    }
+}
+
 template <typename T>
 IterArgs<T> make_args(pr_graph *g)
 {
@@ -425,6 +494,7 @@ IterArgs<T> make_args(pr_graph *g)
     a.perm = g->perm;
     a.order = g->order;
     a.deg_out = g->deg_out;
+    a.w_split = st.w_split;
     a.n = g->n;
     a.n_c = g->n_c;
     a.n_w = g->n_w;
@@ -466,6 +536,19 @@ pr_status prepare(pr_graph *g)
     const int pgrid = st.grid > st.init_grid ? st.grid : st.init_grid;
     if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)pgrid * 2 * sizeof(double))) != PR_OK)
         return r;
+
+    // edge-balanced ranges of warp-class rows, one per warp
+    const int64_t warps = (int64_t)st.grid * (kIterBlock / 32);
+    if ((r = graph_alloc(g, (void **)&st.w_split, (size_t)(warps + 1) * sizeof(int32_t))) != PR_OK)
+        return r;
+    const int64_t w0 = g->n_c, w1 = w0 + g->n_w;
+    const int sg = (int)((warps + 1 + kBlock - 1) / kBlock);
+    k_split<<<sg, kBlock>>>(g->w_ptr, w0, w1, warps, kWarpRowCost, st.w_split);
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_status(e, "splitting the classes");
 
     IterArgs<T> args = make_args<T>(g);
     cudaGraph_t graph = nullptr;

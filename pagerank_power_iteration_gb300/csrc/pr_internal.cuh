@@ -22,6 +22,11 @@ constexpr int kChunkEdges = 512;
 constexpr int kBlock = 256;        // CTA size of the preprocessing kernels
 constexpr int kIterBlock = 1024;   // CTA size of the update kernel (one CTA per SM)
 constexpr int kHotBytes = 160 * 1024;   // shared-memory copy of the state's head
+// Per-row cost, in edges, used to balance warp-class rows over the warps of
+// the update kernel (offset loads, reduction, combine).
+constexpr int kWarpRowCost = 32;
+// Work-CSR entry that pads a row to whole 16-byte loads; it gathers 0.
+constexpr int32_t kPadSource = -1;
 
 enum RowClass : int { kClassZero = 0, kClassThread = 1, kClassWarp = 2, kClassCta = 3 };
 
@@ -54,6 +59,7 @@ struct DtypeState {
     void *hub_partial = nullptr;       // one partial row sum per CTA chunk
     void *stage = nullptr;             // staging for host x_init / ranks_out
     double *block_partials = nullptr;  // [grid][2]: L1 and D partial of each CTA
+    int32_t *w_split = nullptr;        // [warps + 1] warp-class row ranges per warp
     int grid = 0;                      // CTAs of the persistent iteration kernel
     int init_grid = 0;
     int32_t hot = 0;                   // state slots staged in shared memory per update
@@ -78,9 +84,9 @@ struct pr_graph {
     // rows, thread rows, rows without in-edges; ascending ids in a class)
     int32_t *order = nullptr;      // [n] work position -> vertex id
     int32_t *perm = nullptr;       // [n] vertex id -> work position
-    int32_t *w_ptr = nullptr;      // [n + 1] work CSR offsets; CTA and warp rows padded
-                                   // to a multiple of 4 edges (16-byte aligned)
-    int32_t *w_col = nullptr;      // [m_w] work sources; padding entries point at slot n
+    int32_t *w_ptr = nullptr;      // [n + 1] work CSR offsets; rows padded to a multiple
+                                   // of 4 edges (16-byte aligned)
+    int32_t *w_col = nullptr;      // [m_w] work sources; padding entries are kPadSource
     int32_t *w_deg = nullptr;      // [n] out-degrees in work order
     int64_t m_w = 0;               // edges in the work CSR, padding included
 

@@ -32,7 +32,7 @@
 // kept, bit for bit, for pr_get_in_csr) but on the same graph relabelled by
 // that class-major order: vertex v becomes perm[v], row i of the work CSR
 // (w_ptr, w_col) is the in-row of order[i] with every source u replaced by
-// perm[u]. Each class is then a contiguous range of rows and of edges, the
+// perm[u], padded with kPadSource entries to a multiple of 4. Each class is then a contiguous range of rows and of edges, the
 // per-row state is read and written in order, and, since the order leads with
 // in-degree hubs sorted by out-degree, the most gathered values of skewed
 // graphs sit together at the start of the state vector (where the iteration
@@ -88,17 +88,33 @@ __device__ __forceinline__ unsigned long long wait_desc(const unsigned long long
 
 // Sum of everything published before `tile` in one descriptor column (walks
 // back until an inclusive prefix is found). Tile 0 always publishes kFlagP.
+// Four predecessors are read per step, so a walk over aggregate-only tiles
+// costs a quarter of the round trips; a descriptor still unpublished is
+// waited for (bounded) before it is used.
 __device__ long long look_back(const unsigned long long *desc, int64_t tile, int64_t stride,
                                unsigned *err)
 {
     long long prefix = 0;
-    for (int64_t p = tile - 1; p >= 0; --p) {
-        unsigned long long v = wait_desc(desc + p * stride, err);
-        if (v == 0)
-            break;  // timed out: error already flagged
-        prefix += (long long)(v & kValueMask);
-        if ((v >> 62) == 2)
-            break;
+    int64_t p = tile - 1;
+    while (p >= 0) {
+        unsigned long long v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            v[k] = (p - k >= 0) ? load_desc(desc + (p - k) * stride) : 0ull;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (p - k < 0)
+                return prefix;
+            if ((v[k] >> 62) == 0) {
+                v[k] = wait_desc(desc + (p - k) * stride, err);
+                if (v[k] == 0)
+                    return prefix;   // timed out: error already flagged
+            }
+            prefix += (long long)(v[k] & kValueMask);
+            if ((v[k] >> 62) == 2)
+                return prefix;
+        }
+        p -= 4;
     }
     return prefix;
 }
@@ -274,7 +290,8 @@ k_digit_base(const unsigned *__restrict__ hist, int passes, unsigned *__restrict
 //              CSR's col_idx, and position i belongs to the row r with
 //              row_ptr[r] <= i < row_ptr[r+1]. The tile marks the start of
 //              every row that begins inside it and takes a max-scan, so each
-//              position learns its row without a per-key search.
+//              position learns its row without a per-key search. vals_in then
+//              holds the row of every tile's first position (k_tile_rows).
 //   kWriteKeys the keys are written too (not on the last pass).
 //   kHistogram the last pass of the edge sort: the tile, ordered by full key
 //              within each digit bucket, adds each run of equal keys to the
@@ -348,10 +365,12 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     const int64_t base = tile_begin + (int64_t)warp * kWarpSpan;
 
     if (kFlags & kSrcRows) {
-        // row of every position of the tile: mark row starts, then max-scan
+        // row of every position of the tile: mark row starts, then max-scan.
+        // tile_rows (vals_in here) holds the row of each tile's first
+        // position, so [row of first, row of next tile's first] covers the tile.
         if (tid == 0) {
-            s_row_lo = upper_bound(row_ptr, n + 1, tile_begin) - 1;
-            s_row_hi = upper_bound(row_ptr, n + 1, tile_begin + tile_count - 1) - 1;
+            s_row_lo = vals_in[tile];
+            s_row_hi = vals_in[tile + 1];
         }
         for (int j = tid; j < tile_count; j += kBlock)
             s_val[spad(j)] = INT32_MIN;
@@ -361,7 +380,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
             s_val[spad(0)] = (int32_t)rlo;
         __syncthreads();
         for (int64_t r = rlo + 1 + tid; r <= rhi; r += kBlock) {
-            const int64_t p = row_ptr[r] - tile_begin;   // in [1, tile_count) for r in (rlo, rhi]
+            const int64_t p = row_ptr[r] - tile_begin;   // rows starting past the tile are skipped
             if (p > 0 && p < tile_count)
                 atomicMax(&s_val[spad((int)p)], (int32_t)r);
         }
@@ -492,6 +511,18 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     }
 }
 
+// Row of the first position of every radix tile (tile_rows[tiles] = the row
+// of the last edge), one bisection per tile, all in parallel.
+__global__ void k_tile_rows(const int64_t *__restrict__ row_ptr, int64_t n, int64_t m, int64_t tiles,
+                            int32_t *__restrict__ tile_rows)
+{
+    for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t <= tiles;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pos = min(t * kRadixTile, m - 1);
+        tile_rows[t] = (int32_t)(upper_bound(row_ptr, n + 1, pos) - 1);
+    }
+}
+
 // ---------------------------------------------------------------- step 4 --
 
 constexpr int kScanItems = 16;
@@ -502,11 +533,11 @@ struct LoadCount {   // element i of an int32 array
     __device__ int32_t operator()(int64_t i) const { return p[i]; }
 };
 
-// Length of work row i: the in-degree of order[i], rounded up to a multiple
-// of 4 for CTA and warp rows so that their edges start 16-byte aligned.
+// Length of work row i: the in-degree of order[i] rounded up to a multiple
+// of 4, so that every row starts 16-byte aligned and is read in whole int4s.
 __device__ __forceinline__ int32_t padded_degree(int32_t deg)
 {
-    return deg > kThreadMax ? ((deg + 3) & ~3) : deg;
+    return (deg + 3) & ~3;
 }
 
 struct LoadOrderDeg {
@@ -645,42 +676,44 @@ __global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *
 }
 
 // The work CSR: w_col[w_ptr[i] + k] = perm[in_col[in_ptr[order[i]] + k]] for
-// k below the in-degree, and n (the zero slot) in the padding. Edge-parallel:
-// each block writes one tile of w_col, finding each entry's work row with one
-// search and a forward walk.
-constexpr int kRelabelItems = 16;
-
+// k below the in-degree, and kPadSource (gathers 0) in the padding. CTA-class rows
+// are copied in their kChunkEdges chunks, one warp per chunk; warp-class rows
+// by one warp each; thread-class rows by one thread each. Rows without
+// in-edges have nothing to copy.
 __global__ void __launch_bounds__(kBlock)
-k_relabel(int64_t n, int64_t m, const int32_t *__restrict__ w_ptr, const int32_t *__restrict__ order,
+k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t rows_end,
+          const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_first,
+          const int32_t *__restrict__ w_ptr, const int32_t *__restrict__ order,
           const int32_t *__restrict__ perm, const int32_t *__restrict__ in_ptr,
           const int32_t *__restrict__ in_col, int32_t *__restrict__ w_col)
 {
-    __shared__ int64_t s_lo, s_hi;
-    const int64_t tile = (int64_t)kBlock * kRelabelItems;
-    for (int64_t j0 = blockIdx.x * tile; j0 < m; j0 += (int64_t)gridDim.x * tile) {
-        const int64_t j1 = min(j0 + tile, m);
-        if (threadIdx.x == 0) {
-            s_lo = upper_bound(w_ptr, n + 1, j0) - 1;
-            s_hi = upper_bound(w_ptr, n + 1, j1 - 1);
-        }
-        __syncthreads();
-        int64_t row = -1, src_base = 0, dst_base = 0, row_end = 0, deg = 0;
-        for (int k = 0; k < kRelabelItems; ++k) {
-            const int64_t j = j0 + (int64_t)k * kBlock + threadIdx.x;
-            if (j >= j1)
-                break;
-            if (row < 0 || j >= row_end) {
-                row = (row < 0) ? row_of(w_ptr, s_lo, s_hi, j) : advance_row(w_ptr, row, j, n);
-                const int32_t v = order[row];
-                dst_base = w_ptr[row];
-                row_end = w_ptr[row + 1];
-                src_base = in_ptr[v];
-                deg = in_ptr[v + 1] - src_base;
-            }
-            const int64_t k_in_row = j - dst_base;
-            w_col[j] = (k_in_row < deg) ? perm[in_col[src_base + k_in_row]] : (int32_t)n;
-        }
-        __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t gtid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    const int64_t gwarp = gtid >> 5, nwarps = nthreads >> 5;
+    for (int64_t c = gwarp; c < n_chunks; c += nwarps) {
+        const int32_t r = chunk_row[c];
+        const int32_t v = order[r];
+        const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
+        const int32_t dst = w_ptr[r], len = w_ptr[r + 1] - dst;
+        const int32_t k0 = (int32_t)(c - chunk_first[r]) * kChunkEdges;
+        const int32_t k1 = min(k0 + kChunkEdges, len);
+        for (int32_t k = k0 + lane; k < k1; k += 32)
+            w_col[dst + k] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
+    }
+    for (int64_t i = n_c + gwarp; i < wide_end; i += nwarps) {
+        const int32_t v = order[i];
+        const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
+        const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
+        for (int32_t k = lane; k < len; k += 32)
+            w_col[dst + k] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
+    }
+    for (int64_t i = wide_end + gtid; i < rows_end; i += nthreads) {
+        const int32_t v = order[i];
+        const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
+        const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
+        for (int32_t k = 0; k < len; ++k)
+            w_col[dst + k] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
     }
 }
 
@@ -893,11 +926,15 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
             PRK_TRY(tmp.alloc((void **)&vb[i], (size_t)m * sizeof(int32_t)));
         }
         k_digit_base<<<1, kRadixBins, 0, s>>>(hist, passes, dbase);
-        ++g->build_launches;
+        int32_t *tile_rows = nullptr;
+        PRK_TRY(tmp.alloc((void **)&tile_rows, (size_t)(radix_tiles + 1) * sizeof(int32_t)));
+        k_tile_rows<<<grid_for(radix_tiles + 1, kBlock, cap), kBlock, 0, s>>>(d_row_ptr, n, m, radix_tiles,
+                                                                            tile_rows);
+        g->build_launches += 2;
         PRK_CUDA(cudaGetLastError(), "k_digit_base launch");
         for (int p = 0; p < passes; ++p) {
             const int32_t *kin = p == 0 ? d_col : kb[(p - 1) & 1];
-            const int32_t *vin = p == 0 ? nullptr : vb[(p - 1) & 1];
+            const int32_t *vin = p == 0 ? tile_rows : vb[(p - 1) & 1];
             const bool first = p == 0, last = p == passes - 1;
             int32_t *vout = last ? g->in_col : vb[p & 1];
             int32_t *kout = last ? nullptr : kb[p & 1];
@@ -971,12 +1008,6 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     PRK_TRY(check_timeout());
     g->m_w = h_mw;
     PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t)));
-    if (g->m_w > 0) {
-        k_relabel<<<grid_for(g->m_w, kBlock * kRelabelItems, cap), kBlock, 0, s>>>(
-            n, g->m_w, g->w_ptr, g->order, g->perm, g->in_ptr, g->in_col, g->w_col);
-        ++g->build_launches;
-    }
-    PRK_CUDA(cudaGetLastError(), "relabel launch");
 
     // CTA rows (work rows [0, n_c)) -> chunks
     PRK_TRY(graph_alloc(g, (void **)&g->chunk_first, (size_t)(g->n_c + 1) * sizeof(int32_t)));
@@ -995,6 +1026,14 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         k_fill_chunks<<<grid_for(g->n_c, 1, cap), kBlock, 0, s>>>(g->n_c, g->n_chunks, g->chunk_first,
                                                                    g->chunk_row);
     PRK_CUDA(cudaGetLastError(), "chunk launch");
+    if (g->m_w > 0) {
+        k_relabel<<<g->num_sms * 8, kBlock, 0, s>>>(n, g->n_c, g->n_chunks, g->n_c + g->n_w,
+                                                     g->n_c + g->n_w + g->n_t, g->chunk_row,
+                                                     g->chunk_first, g->w_ptr, g->order, g->perm,
+                                                     g->in_ptr, g->in_col, g->w_col);
+        ++g->build_launches;
+    }
+    PRK_CUDA(cudaGetLastError(), "relabel launch");
 
     // sizes for reporting: true in-edges per class, dangling count
     const int64_t c_end = g->n_c + g->n_w + g->n_t;
