@@ -21,8 +21,9 @@
 //   - the combine reads D from device memory (Day 40, "Keep the dangling mass
 //     on the device"), writes s' and accumulates the L1 distance and the next
 //     dangling mass;
-//   - the two reductions go thread -> warp -> CTA -> one fp64 partial per CTA,
-//     and the last CTA to arrive sums the partials in CTA order (Day 40 budget
+//   - the two reductions go thread -> warp -> CTA -> one 64-bit fixed-point
+//     partial per CTA (exact, so the totals do not depend on the order), and
+//     the last CTA to arrive sums the partials (Day 40 budget
 //     of gridDim.x + 1 global writes per reduction; gpu-graph-study T3's "one
 //     atomic per block" ticket).
 // The last CTA also advances the update counter and, when L1 < tol or the
@@ -50,7 +51,7 @@ struct IterArgs {
     uint32_t *hub_arrivals;
     T *s0, *s1;               // state [n + 1], slot n is 0
     T *hub_partial;
-    double *block_partials;
+    unsigned long long *block_partials;   // [grid][2] fixed-point L1 and D of each CTA
     Scalars *scal;
     const int32_t *perm;      // vertex id -> work position (start vector, output)
     const int32_t *order;     // work position -> vertex id
@@ -105,6 +106,51 @@ struct Gather {
     }
 };
 
+// L1 and dangling-mass terms are summed as 64-bit fixed-point integers with
+// kFixBits fraction bits: integer addition is exact and associative, so the
+// totals do not depend on which thread, warp or CTA adds which term, and a run
+// repeats bit for bit. Every term is in [0, 1] and each total is at most 2,
+// so kFixBits = 61 cannot overflow; rounding each term to 2^-61 bounds the
+// error of a total by n * 2^-62 (4e-12 for n = 2^24). The conversion works on
+// the bit pattern (integer ALU only), which keeps fp64 runs off the FP64 pipe.
+constexpr int kFixBits = 61;
+
+__device__ __forceinline__ unsigned long long shift_round(unsigned long long mant, int sh)
+{
+    if (sh >= 0)
+        return mant << sh;
+    sh = -sh;
+    if (sh >= 64)
+        return 0ull;
+    return (mant + (1ull << (sh - 1))) >> sh;
+}
+
+// x >= 0 (and <= 2) to fixed point
+__device__ __forceinline__ unsigned long long to_fixed(float x)
+{
+    const unsigned bits = __float_as_uint(x);
+    const int e = (int)((bits >> 23) & 0xFF);
+    if (e == 0)
+        return 0ull;   // zero or denormal (< 2^-126): below the resolution
+    const unsigned long long mant = (bits & 0x7FFFFFu) | 0x800000u;   // value = mant * 2^(e-150)
+    return shift_round(mant, e - 150 + kFixBits);
+}
+
+__device__ __forceinline__ unsigned long long to_fixed(double x)
+{
+    const unsigned long long bits = (unsigned long long)__double_as_longlong(x);
+    const int e = (int)((bits >> 52) & 0x7FF);
+    if (e == 0)
+        return 0ull;
+    const unsigned long long mant = (bits & 0xFFFFFFFFFFFFFull) | (1ull << 52);   // value = mant * 2^(e-1075)
+    return shift_round(mant, e - 1075 + kFixBits);
+}
+
+__device__ __forceinline__ double from_fixed(unsigned long long f)
+{
+    return (double)f * 0x1p-61;
+}
+
 __device__ __forceinline__ float abs_t(float x) { return fabsf(x); }
 __device__ __forceinline__ double abs_t(double x) { return ::fabs(x); }
 
@@ -112,18 +158,19 @@ __device__ __forceinline__ double abs_t(double x) { return ::fabs(x); }
 template <typename T>
 __device__ __forceinline__ void finish_row(int64_t i, T y, const int32_t *__restrict__ w_deg,
                                            const T *__restrict__ s_old, T *__restrict__ s_new,
-                                           T base, T d, T &l1, T &dm)
+                                           T base, T d, unsigned long long &l1,
+                                           unsigned long long &dm)
 {
     const int32_t deg = w_deg[i];
     const T so = s_old[i];
     const T x_old = deg ? so * T(deg) : so;
     const T x_new = base + d * y;
-    l1 += abs_t(x_new - x_old);
+    l1 += to_fixed(abs_t(x_new - x_old));
     if (deg) {
         __stcs(s_new + i, x_new / T(deg));
     } else {
         __stcs(s_new + i, x_new);
-        dm += x_new;
+        dm += to_fixed(x_new);
     }
 }
 
@@ -132,7 +179,7 @@ __global__ void __launch_bounds__(kIterBlock, 1)
 k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
 {
     extern __shared__ __align__(16) unsigned char s_dyn[];
-    __shared__ double s_redd[32];
+    __shared__ unsigned long long s_redf[32];
     __shared__ int s_flag;
     constexpr int kWarps = kIterBlock / 32;
 
@@ -157,7 +204,7 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     __syncthreads();
     const Gather<T> gat{s_old, s_hot, hot};
 
-    T l1 = T(0), dm = T(0);
+    unsigned long long l1 = 0ull, dm = 0ull;   // fixed point, see to_fixed
 
     // CTA class: rows with more than 1024 in-edges, cut into chunks of
     // kChunkEdges (whole int4s). Warp gw streams the contiguous chunk range
@@ -346,8 +393,8 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     }
 
     // reductions: one fp64 partial pair per CTA, the last CTA sums them
-    const double l1_blk = block_sum((double)l1, s_redd);
-    const double dm_blk = block_sum((double)dm, s_redd);
+    const unsigned long long l1_blk = block_sum(l1, s_redf);
+    const unsigned long long dm_blk = block_sum(dm, s_redf);
     if (tid == 0) {
         __stcg(a.block_partials + 2 * blockIdx.x, l1_blk);
         __stcg(a.block_partials + 2 * blockIdx.x + 1, dm_blk);
@@ -359,14 +406,15 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     if (!s_flag)
         return;
     __threadfence();
-    double L = 0.0, M = 0.0;
+    unsigned long long Lf = 0ull, Mf = 0ull;
     for (int64_t b = tid; b < G; b += kIterBlock) {
-        L += __ldcg(a.block_partials + 2 * b);
-        M += __ldcg(a.block_partials + 2 * b + 1);
+        Lf += __ldcg(a.block_partials + 2 * b);
+        Mf += __ldcg(a.block_partials + 2 * b + 1);
     }
-    L = block_sum(L, s_redd);
-    M = block_sum(M, s_redd);
+    Lf = block_sum(Lf, s_redf);
+    Mf = block_sum(Mf, s_redf);
     if (tid == 0) {
+        const double L = from_fixed(Lf), M = from_fixed(Mf);
         Scalars *sc = a.scal;
         const int it1 = it + 1;
         const bool conv = (sc->tol > 0.0) && (L < sc->tol);
@@ -387,12 +435,12 @@ template <typename T>
 __global__ void __launch_bounds__(kBlock)
 k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_t max_iter)
 {
-    __shared__ double s_redd[32];
+    __shared__ unsigned long long s_redf[32];
     __shared__ int s_flag;
     const int tid = threadIdx.x;
     const int64_t G = gridDim.x;
     const T x_uniform = T(1.0 / (double)a.n);
-    T dm = T(0);
+    unsigned long long dm = 0ull;   // fixed point, see to_fixed
     if (blockIdx.x == 0 && tid == 0) {
         a.s0[a.n] = T(0);   // slot n stays 0 (the shared copy may include it)
         a.s1[a.n] = T(0);
@@ -404,10 +452,10 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
             a.s0[i] = x / T(deg);
         } else {
             a.s0[i] = x;
-            dm += x;
+            dm += to_fixed(x);
         }
     }
-    const double dm_blk = block_sum((double)dm, s_redd);
+    const unsigned long long dm_blk = block_sum(dm, s_redf);
     if (tid == 0) {
         __stcg(a.block_partials + 2 * blockIdx.x + 1, dm_blk);
         __threadfence();
@@ -418,13 +466,13 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
     if (!s_flag)
         return;
     __threadfence();
-    double M = 0.0;
+    unsigned long long Mf = 0ull;
     for (int64_t b = tid; b < G; b += kBlock)
-        M += __ldcg(a.block_partials + 2 * b + 1);
-    M = block_sum(M, s_redd);
+        Mf += __ldcg(a.block_partials + 2 * b + 1);
+    Mf = block_sum(Mf, s_redf);
     if (tid == 0) {
         Scalars *sc = a.scal;
-        sc->dmass = M;
+        sc->dmass = from_fixed(Mf);
         sc->l1 = 0.0;
         sc->d = d;
         sc->tol = tol;
@@ -534,7 +582,7 @@ pr_status prepare(pr_graph *g)
     if ((r = graph_alloc(g, &st.stage, n * sizeof(T))) != PR_OK) return r;
     if ((r = graph_alloc(g, &st.hub_partial, (size_t)(g->n_chunks + 1) * sizeof(T))) != PR_OK) return r;
     const int pgrid = st.grid > st.init_grid ? st.grid : st.init_grid;
-    if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)pgrid * 2 * sizeof(double))) != PR_OK)
+    if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)pgrid * 2 * sizeof(unsigned long long))) != PR_OK)
         return r;
 
     // edge-balanced ranges of warp-class rows, one per warp

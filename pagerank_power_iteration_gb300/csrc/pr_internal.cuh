@@ -58,7 +58,7 @@ struct DtypeState {
                                        // or x for a dangling vertex; slot n stays 0
     void *hub_partial = nullptr;       // one partial row sum per CTA chunk
     void *stage = nullptr;             // staging for host x_init / ranks_out
-    double *block_partials = nullptr;  // [grid][2]: L1 and D partial of each CTA
+    unsigned long long *block_partials = nullptr;  // [grid][2]: fixed-point L1 and D of each CTA
     int32_t *w_split = nullptr;        // [warps + 1] warp-class row ranges per warp
     int grid = 0;                      // CTAs of the persistent iteration kernel
     int init_grid = 0;
