@@ -154,6 +154,38 @@ pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info);
 /* Fills *stats with the statistics of the handle's most recent pr_run. */
 pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
 
+/* Largest `count` that pr_exclusive_scan_noalloc accepts (2^26). */
+#define PR_SCAN_NOALLOC_MAX (1LL << 26)
+
+/*
+ * Exclusive prefix sum of int32 counts into int32 offsets that allocates no
+ * device memory: offsets[i] = counts[0] + ... + counts[i-1] for i in
+ * [0, count], so offsets[count] is the total (the CSR offsets of a degree
+ * array). The pages have no counterpart: this is the library's own
+ * single-pass look-back scan (the one pr_graph_create uses for in_ptr)
+ * offered to callers that must not call cudaMalloc, such as code running
+ * inside a framework that owns all device memory through its own pool, or
+ * work issued while another thread captures a CUDA graph in global capture
+ * mode, where an allocation would invalidate the capture.
+ *   counts   device pointer, `count` int32 values; the total must fit int32
+ *   offsets  device pointer, `count + 1` int32 values (caller-owned)
+ *   count    0 <= count <= PR_SCAN_NOALLOC_MAX; larger counts are rejected
+ *            with PR_ERR_TOO_LARGE and a message
+ * Scratch: the look-back descriptors live in one fixed file-scope device
+ * array sized for PR_SCAN_NOALLOC_MAX elements (about 128 KB), which every
+ * device that loads the library holds until the process exits. The first
+ * call on a device looks up that array's device address
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture. Every call shares the array and clears the
+ * part it uses, so calls that overlap on the GPU (from two host threads, or
+ * on two streams without ordering) race and give wrong results: serialize
+ * them. The call synchronizes `stream` and returns PR_OK,
+ * PR_ERR_INVALID_ARG (NULL or host pointers, count < 0), PR_ERR_TOO_LARGE,
+ * PR_ERR_TIMEOUT or PR_ERR_CUDA. It makes no cudaMalloc or cudaFree call.
+ */
+pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
+                                    void *stream);
+
 /* Frees the handle and all device memory it owns. NULL is ignored. The
  * caller must make sure no work using the handle is still in flight on a
  * stream other than the ones its calls already synchronised. */

@@ -22,7 +22,8 @@ __all__ = [
     "PR_ERR_TOO_LARGE", "PR_ERR_OOM", "PR_ERR_CUDA", "PR_ERR_TIMEOUT", "PR_F32", "PR_F64",
     "PageRankError", "pr_graph_info", "pr_run_stats", "lib", "library_path",
     "pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info", "pr_graph_last_run",
-    "pr_graph_destroy", "pr_last_error", "pr_version", "Graph", "EXPORTED_SYMBOLS",
+    "pr_graph_destroy", "pr_last_error", "pr_version", "pr_exclusive_scan_noalloc",
+    "PR_SCAN_NOALLOC_MAX", "Graph", "EXPORTED_SYMBOLS",
 ]
 
 PR_OK = 0
@@ -37,7 +38,9 @@ PR_F32 = 0
 PR_F64 = 1
 
 EXPORTED_SYMBOLS = ("pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info",
-                    "pr_graph_last_run", "pr_graph_destroy", "pr_last_error", "pr_version")
+                    "pr_graph_last_run", "pr_graph_destroy", "pr_last_error", "pr_version",
+                    "pr_exclusive_scan_noalloc")
+PR_SCAN_NOALLOC_MAX = 1 << 26
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpagerank_gb300.so")
@@ -106,6 +109,8 @@ def lib():
         L.pr_last_error.restype = ctypes.c_char_p
         L.pr_version.argtypes = []
         L.pr_version.restype = ctypes.c_char_p
+        L.pr_exclusive_scan_noalloc.argtypes = [vp, vp, i64, vp]
+        L.pr_exclusive_scan_noalloc.restype = ctypes.c_int
         _lib = L
         return L
 
@@ -150,6 +155,14 @@ def pr_graph_last_run(graph: int) -> dict:
 def pr_graph_destroy(graph: int) -> None:
     if graph:
         lib().pr_graph_destroy(graph)
+
+
+def pr_exclusive_scan_noalloc(counts: int, offsets: int, count: int, stream: int | None = None) -> None:
+    """Raw call: device pointers as integers. offsets[i] = sum of counts[:i], i in [0, count].
+
+    Allocates no device memory (static scratch for up to PR_SCAN_NOALLOC_MAX
+    elements, shared by all calls: do not overlap calls on the GPU)."""
+    _check(lib().pr_exclusive_scan_noalloc(counts, offsets, count, stream))
 
 
 def pr_last_error() -> str:

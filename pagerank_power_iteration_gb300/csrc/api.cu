@@ -290,6 +290,12 @@ PR_API void pr_graph_destroy(pr_graph *g)
     free_graph(g);
 }
 
+PR_API pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
+                                           void *stream)
+{
+    return prk::exclusive_scan_noalloc(counts, offsets, count, (cudaStream_t)stream);
+}
+
 PR_API const char *pr_last_error(void) { return prk::g_last_error; }
 
 PR_API const char *pr_version(void) { return "pagerank-gb300 0.1 (sm_103a)"; }

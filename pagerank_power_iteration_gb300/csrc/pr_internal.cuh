@@ -126,6 +126,11 @@ bool is_device_pointer(const void *p);
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col,
                       cudaStream_t s);
 
+// Allocation-free exclusive scan (transpose.cu).
+pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
+                                 cudaStream_t s);
+constexpr int kMaxDevices = 64;
+
 // Iteration (iterate.cu).
 pr_status run(pr_graph *g, double d, double tol, int32_t max_iter, int dtype,
               void *ranks_out, const void *x_init, int32_t *iters_out, double *l1_out,

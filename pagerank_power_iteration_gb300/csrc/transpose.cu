@@ -46,6 +46,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pr_internal.cuh"
 
 namespace prk {
@@ -827,6 +829,94 @@ void launch_pass(int64_t tiles, cudaStream_t s, const int32_t *kin, const int32_
         kin, vin, row_ptr, n, kout, vout, in_deg, count, shift, dbase, desc, counter, err);
 }
 
+// ------------------------------------------- allocation-free scan ---
+
+// The scratch of pr_exclusive_scan_noalloc: the look-back descriptors of up
+// to kNoAllocScanTiles tiles, then the tile counter, then the error word. It
+// is a file-scope device array, so every device that loads the library holds
+// these bytes until the process exits, and every call shares them.
+constexpr int64_t kNoAllocScanMax = PR_SCAN_NOALLOC_MAX;
+constexpr int64_t kNoAllocScanTiles = (kNoAllocScanMax + kScanTile - 1) / kScanTile;
+static __device__ __align__(256) unsigned long long g_noalloc_scan_scratch[kNoAllocScanTiles + 2];
+
+}  // namespace
+
+// Device address of g_noalloc_scan_scratch on the current device, looked up
+// once per device (the array's name is only a host-side stand-in in host code).
+static pr_status noalloc_scratch(unsigned long long **out)
+{
+    static std::mutex mu;
+    static unsigned long long *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(PR_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scan_scratch);
+        if (e != cudaSuccess)
+            return cuda_status(e, "cudaGetSymbolAddress of the scan scratch");
+        addr[dev] = static_cast<unsigned long long *>(p);
+    }
+    *out = addr[dev];
+    return PR_OK;
+}
+
+pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
+                                 cudaStream_t s)
+{
+    if (count < 0)
+        return set_error(PR_ERR_INVALID_ARG, "count must be >= 0 (got %lld)", (long long)count);
+    if (count > kNoAllocScanMax)
+        return set_error(PR_ERR_TOO_LARGE,
+                         "count = %lld exceeds the %lld elements the static scratch of "
+                         "pr_exclusive_scan_noalloc is sized for",
+                         (long long)count, (long long)kNoAllocScanMax);
+    if (offsets == nullptr || (count > 0 && counts == nullptr))
+        return set_error(PR_ERR_INVALID_ARG, "NULL pointer");
+    if (!is_device_pointer(offsets) || (count > 0 && !is_device_pointer(counts)))
+        return set_error(PR_ERR_INVALID_ARG, "counts and offsets must be device memory");
+    unsigned long long *scratch = nullptr;
+    pr_status st = noalloc_scratch(&scratch);
+    if (st != PR_OK)
+        return st;
+    cudaError_t e;
+    if (count == 0) {
+        e = cudaMemsetAsync(offsets, 0, sizeof(int32_t), s);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(s);
+        return e == cudaSuccess ? PR_OK : cuda_status(e, "pr_exclusive_scan_noalloc");
+    }
+    const int64_t tiles = (count + kScanTile - 1) / kScanTile;
+    unsigned long long *desc = scratch;
+    unsigned *counter = reinterpret_cast<unsigned *>(scratch + kNoAllocScanTiles);
+    unsigned *err = reinterpret_cast<unsigned *>(scratch + kNoAllocScanTiles + 1);
+    // what the scan expects to start at zero: the descriptors it will use,
+    // the tile counter and the error word (the previous call's values remain)
+    e = cudaMemsetAsync(desc, 0, (size_t)tiles * sizeof(unsigned long long), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(scratch + kNoAllocScanTiles, 0, 2 * sizeof(unsigned long long), s);
+    if (e != cudaSuccess)
+        return cuda_status(e, "clearing the scan scratch");
+    k_scan_excl<LoadCount><<<(unsigned)tiles, kBlock, 0, s>>>(LoadCount{counts}, offsets, count, desc,
+                                                             counter, err);
+    e = cudaGetLastError();
+    unsigned herr = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&herr, err, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_status(e, "pr_exclusive_scan_noalloc");
+    if (herr & kErrTimeout)
+        return set_error(PR_ERR_TIMEOUT, "a look-back wait in the scan gave up");
+    return PR_OK;
+}
+
+namespace {
 }  // namespace
 
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, cudaStream_t s)
