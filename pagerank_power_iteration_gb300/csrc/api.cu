@@ -129,6 +129,7 @@ PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
     if (e != cudaSuccess)
         return prk::cuda_status(e, "cudaGetDevice");
 
+    prk::NvtxRange range("pr_graph_create");
     pr_graph *g = new (std::nothrow) pr_graph();
     if (!g)
         return set_error(PR_ERR_OOM, "host allocation failed");

@@ -667,16 +667,20 @@ pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *r
 
     e = cudaEventRecord(g->ev[0], s);
     if (e == cudaSuccess) {
+        NvtxRange range("pr_init");
         k_init<T><<<st.init_grid, kBlock, 0, s>>>(args, xi, d, tol, max_iter);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess)
         e = cudaEventRecord(g->ev[1], s);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess) {
+        NvtxRange range("pr_iterate");
         e = cudaGraphLaunch(st.exec, s);
+    }
     if (e == cudaSuccess)
         e = cudaEventRecord(g->ev[2], s);
     if (e == cudaSuccess) {
+        NvtxRange range("pr_output");
         const int og = (int)((g->n + kBlock - 1) / kBlock < 8 * g->num_sms
                                  ? (g->n + kBlock - 1) / kBlock : 8 * g->num_sms);
         k_output<T><<<og, kBlock, 0, s>>>(args, out);

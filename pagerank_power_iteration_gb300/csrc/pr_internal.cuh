@@ -7,6 +7,8 @@
 
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pagerank.h"
 
 namespace prk {
@@ -111,6 +113,14 @@ struct pr_graph {
 };
 
 namespace prk {
+
+// NVTX range for the duration of a scope (header-only NVTX; costs nothing
+// unless a tool such as Nsight Compute is attached). Ranges: "pr_graph_create",
+// "pr_init", "pr_iterate" (the CUDA-graph loop of updates), "pr_output".
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // Error reporting (api.cu).
 pr_status set_error(pr_status st, const char *fmt, ...);
