@@ -47,7 +47,12 @@ extern "C" {
 
 /* Opaque handle. Owns device memory: the in-edge CSR, per-vertex out-degrees,
  * the in-degree class lists and, after the first pr_run of a precision, that
- * precision's iteration state and its instantiated CUDA graph. */
+ * precision's iteration state and its instantiated CUDA graph.
+ *
+ * Device memory (handle-owned and the build's scratch) comes from one
+ * stream-ordered memory pool per device that the library creates on first
+ * use and never trims: pr_graph_destroy returns a handle's memory to that
+ * pool, where later handles reuse it, and the process keeps it until exit. */
 typedef struct pr_graph pr_graph;
 
 typedef enum pr_status {
@@ -186,7 +191,8 @@ pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
 pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
                                     void *stream);
 
-/* Frees the handle and all device memory it owns. NULL is ignored. The
+/* Frees the handle and returns all device memory it owns to the library's
+ * pool (see the handle's description). NULL is ignored. The
  * caller must make sure no work using the handle is still in flight on a
  * stream other than the ones its calls already synchronised. */
 void pr_graph_destroy(pr_graph *g);

@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "pr_internal.cuh"
@@ -33,19 +34,72 @@ pr_status cuda_status(cudaError_t e, const char *what)
                      what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
-pr_status graph_alloc(pr_graph *g, void **p, size_t bytes)
+// Device memory comes from one stream-ordered pool per device, owned by the
+// library, that keeps freed blocks for reuse (release threshold: never). A
+// graph built after another one was destroyed reuses its memory instead of
+// paying cudaMalloc and cudaFree (which synchronises the device) again. The
+// pool holds its peak size until the process exits.
+static pr_status device_pool(cudaMemPool_t *out)
+{
+    static std::mutex mu;
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(PR_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (pools[dev] == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess)
+            return cuda_status(e, "cudaMemPoolCreate");
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess)
+            return cuda_status(e, "cudaMemPoolSetAttribute");
+        pools[dev] = pool;
+    }
+    *out = pools[dev];
+    return PR_OK;
+}
+
+pr_status pool_alloc(void **p, size_t bytes, cudaStream_t s)
 {
     if (bytes == 0)
         bytes = 16;
-    cudaError_t e = cudaMalloc(p, bytes);
+    cudaMemPool_t pool;
+    pr_status st = device_pool(&pool);
+    if (st != PR_OK)
+        return st;
+    cudaError_t e = cudaMallocFromPoolAsync(p, bytes, pool, s);
     if (e != cudaSuccess) {
         *p = nullptr;
         cudaGetLastError();
         return set_error(e == cudaErrorMemoryAllocation ? PR_ERR_OOM : PR_ERR_CUDA,
-                         "cudaMalloc of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
+                         "device allocation of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
     }
+    return PR_OK;
+}
+
+void pool_free(void *p, cudaStream_t s)
+{
+    if (p)
+        cudaFreeAsync(p, s);
+}
+
+pr_status graph_alloc(pr_graph *g, void **p, size_t bytes, cudaStream_t s)
+{
+    pr_status st = pool_alloc(p, bytes, s);
+    if (st != PR_OK)
+        return st;
     g->allocs.push_back(*p);
-    g->device_bytes += (int64_t)bytes;
+    g->device_bytes += (int64_t)(bytes ? bytes : 16);
     return PR_OK;
 }
 
@@ -94,8 +148,10 @@ void free_graph(pr_graph *g)
     for (cudaEvent_t &ev : g->ev)
         if (ev)
             cudaEventDestroy(ev);
+    // no work on the handle is in flight (its calls synchronised their
+    // streams), so the blocks can go back to the pool in default-stream order
     for (void *p : g->allocs)
-        cudaFree(p);
+        prk::pool_free(p, 0);
     if (g->h_scal)
         cudaFreeHost(g->h_scal);
     delete g;
@@ -148,8 +204,8 @@ PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
         if (e != cudaSuccess) { st = prk::cuda_status(e, "cudaEventCreate"); break; }
         e = cudaMallocHost((void **)&g->h_scal, sizeof(prk::Scalars));
         if (e != cudaSuccess) { st = prk::cuda_status(e, "cudaMallocHost"); break; }
-        if ((st = prk::graph_alloc(g, (void **)&g->scal, sizeof(prk::Scalars))) != PR_OK) break;
-        if ((st = prk::graph_alloc(g, (void **)&g->err, sizeof(unsigned))) != PR_OK) break;
+        if ((st = prk::graph_alloc(g, (void **)&g->scal, sizeof(prk::Scalars), s)) != PR_OK) break;
+        if ((st = prk::graph_alloc(g, (void **)&g->err, sizeof(unsigned), s)) != PR_OK) break;
         e = cudaMemsetAsync(g->scal, 0, sizeof(prk::Scalars), s);
         if (e != cudaSuccess) { st = prk::cuda_status(e, "memset"); break; }
 
@@ -181,29 +237,26 @@ PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
         const int64_t *d_rp = row_ptr;
         const int32_t *d_ci = col_idx;
         if (!rp_dev) {
-            e = cudaMalloc(&rp_stage, (size_t)(n + 1) * sizeof(int64_t));
-            if (e == cudaSuccess)
+            st = prk::pool_alloc(&rp_stage, (size_t)(n + 1) * sizeof(int64_t), s);
+            if (st == PR_OK)
                 e = cudaMemcpyAsync(rp_stage, row_ptr, (size_t)(n + 1) * sizeof(int64_t),
                                     cudaMemcpyHostToDevice, s);
             d_rp = (const int64_t *)rp_stage;
         }
-        if (e == cudaSuccess && !ci_dev) {
-            e = cudaMalloc(&ci_stage, (size_t)m * sizeof(int32_t));
-            if (e == cudaSuccess)
+        if (st == PR_OK && e == cudaSuccess && !ci_dev) {
+            st = prk::pool_alloc(&ci_stage, (size_t)m * sizeof(int32_t), s);
+            if (st == PR_OK)
                 e = cudaMemcpyAsync(ci_stage, col_idx, (size_t)m * sizeof(int32_t),
                                     cudaMemcpyHostToDevice, s);
             d_ci = (const int32_t *)ci_stage;
         }
-        if (e != cudaSuccess) {
+        if (st == PR_OK && e != cudaSuccess)
             st = prk::cuda_status(e, "staging the input CSR");
-        } else {
+        if (st == PR_OK)
             st = prk::build_graph(g, d_rp, d_ci, s);
-        }
+        prk::pool_free(rp_stage, s);
+        prk::pool_free(ci_stage, s);
         cudaError_t se = cudaStreamSynchronize(s);
-        if (rp_stage)
-            cudaFree(rp_stage);
-        if (ci_stage)
-            cudaFree(ci_stage);
         if (st == PR_OK && se != cudaSuccess)
             st = prk::cuda_status(se, "pr_graph_create");
     } while (0);

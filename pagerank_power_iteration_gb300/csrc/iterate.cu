@@ -555,7 +555,7 @@ IterArgs<T> make_args(pr_graph *g)
 // Allocates a precision's state and builds its graph: one conditional WHILE
 // node whose body is one k_iterate launch.
 template <typename T>
-pr_status prepare(pr_graph *g)
+pr_status prepare(pr_graph *g, cudaStream_t s)
 {
     DtypeState &st = g->st[sizeof(T) == 8 ? 1 : 0];
     if (st.ready)
@@ -577,24 +577,24 @@ pr_status prepare(pr_graph *g)
     st.grid = per_sm * g->num_sms;
     st.init_grid = 8 * g->num_sms;
     const size_t n = (size_t)g->n;
-    if ((r = graph_alloc(g, &st.s[0], (n + 1) * sizeof(T))) != PR_OK) return r;
-    if ((r = graph_alloc(g, &st.s[1], (n + 1) * sizeof(T))) != PR_OK) return r;
-    if ((r = graph_alloc(g, &st.stage, n * sizeof(T))) != PR_OK) return r;
-    if ((r = graph_alloc(g, &st.hub_partial, (size_t)(g->n_chunks + 1) * sizeof(T))) != PR_OK) return r;
+    if ((r = graph_alloc(g, &st.s[0], (n + 1) * sizeof(T), s)) != PR_OK) return r;
+    if ((r = graph_alloc(g, &st.s[1], (n + 1) * sizeof(T), s)) != PR_OK) return r;
+    if ((r = graph_alloc(g, &st.stage, n * sizeof(T), s)) != PR_OK) return r;
+    if ((r = graph_alloc(g, &st.hub_partial, (size_t)(g->n_chunks + 1) * sizeof(T), s)) != PR_OK) return r;
     const int pgrid = st.grid > st.init_grid ? st.grid : st.init_grid;
-    if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)pgrid * 2 * sizeof(unsigned long long))) != PR_OK)
+    if ((r = graph_alloc(g, (void **)&st.block_partials, (size_t)pgrid * 2 * sizeof(unsigned long long), s)) != PR_OK)
         return r;
 
     // edge-balanced ranges of warp-class rows, one per warp
     const int64_t warps = (int64_t)st.grid * (kIterBlock / 32);
-    if ((r = graph_alloc(g, (void **)&st.w_split, (size_t)(warps + 1) * sizeof(int32_t))) != PR_OK)
+    if ((r = graph_alloc(g, (void **)&st.w_split, (size_t)(warps + 1) * sizeof(int32_t), s)) != PR_OK)
         return r;
     const int64_t w0 = g->n_c, w1 = w0 + g->n_w;
     const int sg = (int)((warps + 1 + kBlock - 1) / kBlock);
-    k_split<<<sg, kBlock>>>(g->w_ptr, w0, w1, warps, kWarpRowCost, st.w_split);
+    k_split<<<sg, kBlock, 0, s>>>(g->w_ptr, w0, w1, warps, kWarpRowCost, st.w_split);
     e = cudaGetLastError();
     if (e == cudaSuccess)
-        e = cudaDeviceSynchronize();
+        e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_status(e, "splitting the classes");
 
@@ -643,7 +643,7 @@ template <typename T>
 pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *ranks_out,
                     const void *x_init, int32_t *iters_out, double *l1_out, cudaStream_t s)
 {
-    pr_status r = prepare<T>(g);
+    pr_status r = prepare<T>(g, s);
     if (r != PR_OK)
         return r;
     DtypeState &st = g->st[sizeof(T) == 8 ? 1 : 0];

@@ -126,8 +126,11 @@ struct NvtxRange {
 pr_status set_error(pr_status st, const char *fmt, ...);
 pr_status cuda_status(cudaError_t e, const char *what);
 
-// Device allocation owned by the handle (api.cu).
-pr_status graph_alloc(pr_graph *g, void **p, size_t bytes);
+// Device memory from the library's stream-ordered pool (api.cu); graph_alloc
+// records the block as owned by the handle (freed by pr_graph_destroy).
+pr_status pool_alloc(void **p, size_t bytes, cudaStream_t s);
+void pool_free(void *p, cudaStream_t s);
+pr_status graph_alloc(pr_graph *g, void **p, size_t bytes, cudaStream_t s);
 
 // True if p can be dereferenced by the current device as device memory.
 bool is_device_pointer(const void *p);

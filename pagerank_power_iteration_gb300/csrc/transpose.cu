@@ -6,13 +6,15 @@
 // CUDA" (section "One iteration, three shapes of work": a histogram, a prefix
 // sum and a scatter), done on the GPU:
 //   1. k_outdeg      out-degrees, row_ptr validation, dangling count
-//   2. k_digit_hist  col_idx validation and the 256-bin digit counts of every
-//                    radix pass (one read of the edges)
-//   3. the stable scatter, as a least-significant-digit radix sort of the
-//      edges by destination with 8-bit digits (k_radix_pass). Each pass is
-//      itself a counting sort over 256 bins: per-warp shared-memory digit
-//      counts, decoupled look-back across tiles, and a rank-preserving scatter
-//      staged through shared memory so that the stores are coalesced. Stable
+//   2. + 3. the stable scatter, as a least-significant-digit radix sort of
+//      the edges by destination with 8-bit digits. Each pass is itself a
+//      counting sort over 256 bins in reduce-then-scan form: k_radix_upsweep
+//      counts the digits of every tile (the first one also checks col_idx),
+//      one exclusive scan of those counts in digit-major order gives every
+//      (digit, tile) its output position, and k_radix_pass ranks each tile
+//      with per-warp shared-memory counters and scatters it, staged through
+//      shared memory so that the stores are coalesced. No tile waits for
+//      another. Stable
 //      passes keep the edges into one vertex in out-edge CSR order, i.e. with
 //      ascending sources. The first pass derives each edge's source from
 //      row_ptr as it loads the edge; the last pass also produces the
@@ -39,10 +41,11 @@
 // keeps a copy in shared memory). Rows above 1024 in-edges are cut into
 // fixed-size edge chunks.
 //
-// Every wait in this file (the look-backs) is bounded: after kSpinLimit polls
-// it sets kErrTimeout in the error word and moves on, the host stops the
-// build at the next check, and every store whose offset came out of a
-// look-back is range-checked, so no launch can hang or write out of bounds.
+// Every wait in this file (the scans' look-backs) is bounded: after
+// kSpinLimit polls it sets kErrTimeout in the error word and moves on, the
+// host stops the build at the next check, and every store whose offset came
+// out of a scan is range-checked, so no launch can hang or write out of
+// bounds.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -220,72 +223,59 @@ constexpr int kRadixBits = 8;
 constexpr int kRadixBins = 1 << kRadixBits;
 constexpr int kRadixItems = 8;
 constexpr int kRadixTile = kBlock * kRadixItems;
-constexpr int kMaxPasses = 4;
 
-// The digit counts of every pass, and (n > 0) a range check of every key
-// against [0, n).
+// Upsweep of one counting-sort pass: the 256 digit counts of every tile,
+// written digit-major (counts[d * tiles + t]), so that one exclusive scan of
+// the whole array gives every (digit, tile) its output position. With n > 0
+// every key is also checked against [0, n); a bad key is still counted, so
+// the downsweep's positions stay a permutation of [0, count) and the build
+// stops on the error flag before any later step reads them.
 __global__ void __launch_bounds__(kBlock)
-k_digit_hist(const int32_t *__restrict__ keys, int64_t count, int64_t n, int passes,
-             unsigned *__restrict__ hist, unsigned *err)
+k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int shift,
+                int32_t *__restrict__ counts, int64_t tiles, unsigned *err)
 {
-    __shared__ unsigned s_h[kMaxPasses][kRadixBins];
-    for (int i = threadIdx.x; i < kMaxPasses * kRadixBins; i += kBlock)
-        (&s_h[0][0])[i] = 0;
+    constexpr int kWarps = kBlock / 32;
+    __shared__ unsigned s_h[kWarps][kRadixBins];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int w = 0; w < kWarps; ++w)
+        s_h[w][tid] = 0;
     __syncthreads();
+    const int64_t tile = blockIdx.x;
+    const int64_t begin = tile * kRadixTile;
     bool bad = false;
-    for (int64_t i = blockIdx.x * (int64_t)kBlock + threadIdx.x; i < count;
-         i += (int64_t)gridDim.x * kBlock) {
-        const int32_t v = keys[i];
-        if (n > 0 && (v < 0 || (int64_t)v >= n)) {
-            bad = true;
-            continue;
+#pragma unroll
+    for (int k = 0; k < kRadixItems; ++k) {
+        const int64_t i = begin + (int64_t)k * kBlock + tid;
+        if (i < count) {
+            const int32_t v = keys[i];
+            bad |= n > 0 && (v < 0 || (int64_t)v >= n);
+            atomicAdd(&s_h[warp][((unsigned)v >> shift) & (kRadixBins - 1)], 1u);
         }
-        for (int p = 0; p < passes; ++p)
-            atomicAdd(&s_h[p][((unsigned)v >> (p * kRadixBits)) & (kRadixBins - 1)], 1u);
     }
     if (bad)
         atomicOr(err, kErrColIdx);
     __syncthreads();
-    for (int p = 0; p < passes; ++p) {
-        const unsigned c = s_h[p][threadIdx.x];
-        if (c)
-            atomicAdd(&hist[p * kRadixBins + threadIdx.x], c);
-    }
-}
-
-// Exclusive scan of each pass's 256 digit counts: where each digit's bucket starts.
-__global__ void __launch_bounds__(kRadixBins)
-k_digit_base(const unsigned *__restrict__ hist, int passes, unsigned *__restrict__ base)
-{
-    __shared__ unsigned s_w[kRadixBins / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int p = 0; p < passes; ++p) {
-        const unsigned c = hist[p * kRadixBins + threadIdx.x];
-        const unsigned incl = warp_incl_scan(c, lane);
-        if (lane == 31)
-            s_w[warp] = incl;
-        __syncthreads();
-        unsigned off = 0;
-        for (int w = 0; w < warp; ++w)
-            off += s_w[w];
-        base[p * kRadixBins + threadIdx.x] = off + incl - c;
-        __syncthreads();
-    }
+    unsigned c = 0;
+    for (int w = 0; w < kWarps; ++w)
+        c += s_h[w][tid];
+    counts[(int64_t)tid * tiles + tile] = (int32_t)c;
 }
 
 // ---------------------------------------------------------------- step 3 --
 
-// One stable counting-sort pass over digit (key >> shift) & 255.
+// Downsweep of one stable counting-sort pass over digit (key >> shift) & 255.
+// `offsets` is the exclusive scan of the upsweep's digit-major tile counts:
+// offsets[d * tiles + t] is where tile t's keys of digit d go, so tiles are
+// independent and none waits for another.
 //
 // Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
 // walks them in 32-key rounds, so "earlier round, then lower lane" is input
 // order. In each round __match_any_sync groups lanes with equal digits; a
 // per-warp shared counter carries each digit's running count across rounds.
 // Per-warp counts are then scanned across warps (and across digits for the
-// tile-local order), the tile is staged in shared memory in (digit, input)
-// order, and the prefix over earlier tiles comes from a per-digit look-back.
-// The write-out walks the staged tile linearly, so a warp stores consecutive
-// addresses of one bucket.
+// tile-local order) and the tile is staged in shared memory in (digit,
+// input) order. The write-out walks the staged tile linearly, so a warp
+// stores consecutive addresses of one bucket.
 //
 // kFlags:
 //   kSrcRows   the values are the edges' sources: the input is the out-edge
@@ -339,8 +329,7 @@ __global__ void __launch_bounds__(kBlock, 4)
 k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ vals_in,
              const int64_t *__restrict__ row_ptr, int64_t n, int32_t *__restrict__ keys_out,
              int32_t *__restrict__ vals_out, int32_t *__restrict__ in_deg, int64_t count,
-             int shift, const unsigned *__restrict__ digit_base, unsigned long long *desc,
-             unsigned *tile_counter, unsigned *err)
+             int shift, const int32_t *__restrict__ offsets, int64_t tiles)
 {
     constexpr int kWarps = kBlock / 32;
     constexpr int kWarpSpan = 32 * kRadixItems;
@@ -353,15 +342,14 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     __shared__ int32_t s_key[kPadTile];
     __shared__ int32_t s_val[kPadTile];             // also the row map of kSrcRows
     __shared__ int64_t s_row_lo, s_row_hi;
-    __shared__ unsigned s_tile;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        s_tile = atomicAdd(tile_counter, 1u);
     for (int w = 0; w < kWarps; ++w)
         s_wh[w][tid] = 0;
+    const int64_t tile = blockIdx.x;
+    // where this tile's run of each digit starts in the output
+    s_base[tid] = (unsigned)offsets[(int64_t)tid * tiles + tile];
     __syncthreads();
-    const int64_t tile = s_tile;
     const int64_t tile_begin = tile * kRadixTile;
     const int tile_count = (int)min((int64_t)kRadixTile, count - tile_begin);
     const int64_t base = tile_begin + (int64_t)warp * kWarpSpan;
@@ -420,16 +408,14 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     }
     __syncthreads();
 
-    // thread tid owns digit tid: exclusive offsets of the warps, the tile
-    // count, published at once so that later tiles can look back past us
+    // thread tid owns digit tid: exclusive offsets of the warps, and the
+    // tile's count
     unsigned tot = 0;
     for (int w = 0; w < kWarps; ++w) {
         const unsigned c = s_wh[w][tid];
         s_wh[w][tid] = tot;
         tot += c;
     }
-    unsigned long long *my = desc + tile * kRadixBins + tid;
-    store_desc(my, (tile == 0 ? kFlagP : kFlagA) | tot);
 
     // tile-local start of each digit (exclusive scan over the 256 digits)
     const unsigned incl = warp_incl_scan(tot, lane);
@@ -453,13 +439,6 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         }
     }
 
-    // prefix over earlier tiles
-    long long prefix = 0;
-    if (tile > 0) {
-        prefix = look_back(desc + tid, tile, kRadixBins, err);
-        store_desc(my, kFlagP | (unsigned long long)(prefix + tot));
-    }
-    s_base[tid] = digit_base[tid] + (unsigned)prefix;
     __syncthreads();
 
     // write-out: consecutive staged entries of one digit go to consecutive addresses
@@ -470,7 +449,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
             const int32_t kv = s_key[spad(i)];
             const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
             const int64_t pos = (int64_t)s_base[dig] + (i - (int)s_start[dig]);
-            if (pos < 0 || pos >= count)   // only reachable after a look-back timeout
+            if (pos < 0 || pos >= count)   // only reachable if the offsets scan failed
                 continue;
             vals_out[pos] = s_val[spad(i)];
             if (kFlags & kWriteKeys)
@@ -768,26 +747,23 @@ int grid_for(int64_t items, int per_block, int cap)
     return (int)g;
 }
 
-// Scratch of one build, released when the build returns.
+// Scratch of one build, returned to the pool in stream order when the build
+// returns.
 struct Scratch {
+    cudaStream_t s;
     std::vector<void *> ptrs;
+    explicit Scratch(cudaStream_t stream) : s(stream) {}
     ~Scratch()
     {
         for (void *p : ptrs)
-            cudaFree(p);
+            pool_free(p, s);
     }
     pr_status alloc(void **p, size_t bytes)
     {
-        if (bytes == 0)
-            bytes = 16;
-        cudaError_t e = cudaMalloc(p, bytes);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return set_error(e == cudaErrorMemoryAllocation ? PR_ERR_OOM : PR_ERR_CUDA,
-                             "cudaMalloc of %zu bytes failed: %s", bytes, cudaGetErrorString(e));
-        }
-        ptrs.push_back(*p);
-        return PR_OK;
+        pr_status st = pool_alloc(p, bytes, s);
+        if (st == PR_OK)
+            ptrs.push_back(*p);
+        return st;
     }
 };
 
@@ -819,14 +795,29 @@ pr_status read_err(pr_graph *g, cudaStream_t s, unsigned *out)
     return e == cudaSuccess ? PR_OK : cuda_status(e, "reading the error word");
 }
 
+// One counting-sort pass: upsweep (digit counts per tile), one exclusive
+// scan of the digit-major counts, downsweep (rank and scatter).
 template <unsigned kFlags>
-void launch_pass(int64_t tiles, cudaStream_t s, const int32_t *kin, const int32_t *vin,
-                 const int64_t *row_ptr, int64_t n, int32_t *kout, int32_t *vout, int32_t *in_deg,
-                 int64_t count, int shift, const unsigned *dbase, unsigned long long *desc,
-                 unsigned *counter, unsigned *err)
+pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32_t *vin,
+                    const int64_t *row_ptr, int64_t n, int32_t *kout, int32_t *vout, int32_t *in_deg,
+                    int64_t count, int shift, int64_t validate_n, int32_t *counts, int32_t *offsets,
+                    unsigned long long *desc, unsigned *counter)
 {
-    k_radix_pass<kFlags><<<(unsigned)tiles, kBlock, 0, s>>>(
-        kin, vin, row_ptr, n, kout, vout, in_deg, count, shift, dbase, desc, counter, err);
+    const int64_t tiles = (count + kRadixTile - 1) / kRadixTile;
+    k_radix_upsweep<<<(unsigned)tiles, kBlock, 0, s>>>(kin, count, validate_n, shift, counts, tiles, g->err);
+    ++g->build_launches;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_status(e, "k_radix_upsweep launch");
+    pr_status st = launch_scan(LoadCount{counts}, offsets, tiles * kRadixBins, desc, counter, g->err,
+                               &g->build_launches, s);
+    if (st != PR_OK)
+        return st;
+    k_radix_pass<kFlags><<<(unsigned)tiles, kBlock, 0, s>>>(kin, vin, row_ptr, n, kout, vout, in_deg,
+                                                           count, shift, offsets, tiles);
+    ++g->build_launches;
+    e = cudaGetLastError();
+    return e == cudaSuccess ? PR_OK : cuda_status(e, "k_radix_pass launch");
 }
 
 // ------------------------------------------- allocation-free scan ---
@@ -925,7 +916,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     const int cap = g->num_sms * 32;
     pr_status st;
     cudaError_t e;
-    Scratch tmp;
+    Scratch tmp(s);
 
 #define PRK_TRY(expr)             \
     do {                          \
@@ -941,13 +932,13 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     } while (0)
 
     // handle-owned buffers: the in-edge CSR and the work layout
-    PRK_TRY(graph_alloc(g, (void **)&g->in_ptr, (size_t)(n + 1) * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->in_col, (size_t)(m + 4) * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->deg_out, (size_t)n * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->order, (size_t)n * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->perm, (size_t)n * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->w_ptr, (size_t)(n + 1) * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->w_deg, (size_t)n * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->in_ptr, (size_t)(n + 1) * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->in_col, (size_t)(m + 4) * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->deg_out, (size_t)n * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->order, (size_t)n * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->perm, (size_t)n * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->w_ptr, (size_t)(n + 1) * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->w_deg, (size_t)n * sizeof(int32_t), s));
 
     int bits = 0;
     while (bits < 31 && ((int64_t)1 << bits) < n)
@@ -958,43 +949,36 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
 
     // scratch
     int32_t *in_deg = nullptr;
-    unsigned long long *counters = nullptr;   // [0] = dangling
-    unsigned *tile_counter = nullptr, *hist = nullptr, *dbase = nullptr;
+    unsigned long long *counters = nullptr;   // [0] = dangling, [1..3] = class edges
+    unsigned *tile_counter = nullptr;
     unsigned long long *desc = nullptr;
+    int32_t *counts = nullptr, *offsets = nullptr;   // digit-major tile counts and their scan
     PRK_TRY(tmp.alloc((void **)&in_deg, (size_t)n * sizeof(int32_t)));
     PRK_TRY(tmp.alloc((void **)&counters, 8 * sizeof(unsigned long long)));
     PRK_TRY(tmp.alloc((void **)&tile_counter, sizeof(unsigned)));
-    PRK_TRY(tmp.alloc((void **)&hist, 2 * kMaxPasses * kRadixBins * sizeof(unsigned)));
-    dbase = hist + kMaxPasses * kRadixBins;
-    const int64_t scan_tiles = (n + 1 + kScanTile - 1) / kScanTile;
     const int64_t radix_tiles = (m + kRadixTile - 1) / kRadixTile;
     const int64_t order_tiles = (n + kRadixTile - 1) / kRadixTile;
-    int64_t desc_words = scan_tiles;
-    if (radix_tiles * kRadixBins > desc_words)
-        desc_words = radix_tiles * kRadixBins;
-    if (order_tiles * kRadixBins > desc_words)
-        desc_words = order_tiles * kRadixBins;
+    const int64_t max_tiles = radix_tiles > order_tiles ? radix_tiles : order_tiles;
+    const int64_t count_words = max_tiles * kRadixBins;
+    PRK_TRY(tmp.alloc((void **)&counts, (size_t)count_words * sizeof(int32_t)));
+    PRK_TRY(tmp.alloc((void **)&offsets, (size_t)(count_words + 1) * sizeof(int32_t)));
+    int64_t desc_words = (n + 1 + kScanTile - 1) / kScanTile;
+    if ((count_words + kScanTile - 1) / kScanTile > desc_words)
+        desc_words = (count_words + kScanTile - 1) / kScanTile;
     PRK_TRY(tmp.alloc((void **)&desc, (size_t)(desc_words + 1) * sizeof(unsigned long long)));
 
     PRK_CUDA(cudaMemsetAsync(g->err, 0, sizeof(unsigned), s), "memset");
     PRK_CUDA(cudaMemsetAsync(in_deg, 0, (size_t)n * sizeof(int32_t), s), "memset");
     PRK_CUDA(cudaMemsetAsync(counters, 0, 8 * sizeof(unsigned long long), s), "memset");
-    PRK_CUDA(cudaMemsetAsync(hist, 0, kMaxPasses * kRadixBins * sizeof(unsigned), s), "memset");
 
-    // 1 + 2: degrees, validation, digit counts
+    // 1: degrees and row_ptr validation (col_idx is checked by the first upsweep)
     k_outdeg<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, d_row_ptr, g->deg_out, counters, g->err);
     ++g->build_launches;
-    if (m > 0) {
-        k_digit_hist<<<grid_for(m, kBlock * 16, cap), kBlock, 0, s>>>(d_col, m, n, passes, hist, g->err);
-        ++g->build_launches;
-    }
     PRK_CUDA(cudaGetLastError(), "validation launch");
     unsigned herr = 0;
     PRK_TRY(read_err(g, s, &herr));
     if (herr & kErrRowPtr)
         return set_error(PR_ERR_INVALID_GRAPH, "row_ptr is not non-decreasing");
-    if (herr & kErrColIdx)
-        return set_error(PR_ERR_INVALID_GRAPH, "col_idx has an entry outside [0, n)");
 
     // a look-back that gave up leaves garbage offsets: stop before they are used
     auto check_timeout = [&]() -> pr_status {
@@ -1007,46 +991,48 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         return PR_OK;
     };
 
-    // 3: stable scatter by destination (LSD radix over 8-bit digits), which
-    // also yields the in-degree histogram
+    // 2 + 3: stable scatter by destination (LSD radix over 8-bit digits),
+    // which also yields the in-degree histogram
     if (m > 0) {
         int32_t *kb[2] = {nullptr, nullptr}, *vb[2] = {nullptr, nullptr};
         for (int i = 0; i < 2 && i < passes - 1; ++i) {
             PRK_TRY(tmp.alloc((void **)&kb[i], (size_t)m * sizeof(int32_t)));
             PRK_TRY(tmp.alloc((void **)&vb[i], (size_t)m * sizeof(int32_t)));
         }
-        k_digit_base<<<1, kRadixBins, 0, s>>>(hist, passes, dbase);
         int32_t *tile_rows = nullptr;
         PRK_TRY(tmp.alloc((void **)&tile_rows, (size_t)(radix_tiles + 1) * sizeof(int32_t)));
         k_tile_rows<<<grid_for(radix_tiles + 1, kBlock, cap), kBlock, 0, s>>>(d_row_ptr, n, m, radix_tiles,
                                                                             tile_rows);
-        g->build_launches += 2;
-        PRK_CUDA(cudaGetLastError(), "k_digit_base launch");
+        ++g->build_launches;
+        PRK_CUDA(cudaGetLastError(), "k_tile_rows launch");
         for (int p = 0; p < passes; ++p) {
             const int32_t *kin = p == 0 ? d_col : kb[(p - 1) & 1];
             const int32_t *vin = p == 0 ? tile_rows : vb[(p - 1) & 1];
             const bool first = p == 0, last = p == passes - 1;
             int32_t *vout = last ? g->in_col : vb[p & 1];
             int32_t *kout = last ? nullptr : kb[p & 1];
-            PRK_CUDA(cudaMemsetAsync(desc, 0, (size_t)radix_tiles * kRadixBins * sizeof(unsigned long long), s),
-                     "memset");
-            PRK_CUDA(cudaMemsetAsync(tile_counter, 0, sizeof(unsigned), s), "memset");
             const int shift = p * kRadixBits;
-            const unsigned *db = dbase + p * kRadixBins;
+            const int64_t vn = first ? n : 0;   // the first upsweep checks col_idx
             if (first && last)
-                launch_pass<kSrcRows | kHistogram>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout,
-                                                   in_deg, m, shift, db, desc, tile_counter, g->err);
+                st = sort_pass<kSrcRows | kHistogram>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
+                                                      shift, vn, counts, offsets, desc, tile_counter);
             else if (first)
-                launch_pass<kSrcRows | kWriteKeys>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout,
-                                                   in_deg, m, shift, db, desc, tile_counter, g->err);
+                st = sort_pass<kSrcRows | kWriteKeys>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
+                                                      shift, vn, counts, offsets, desc, tile_counter);
             else if (last)
-                launch_pass<kHistogram>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
-                                        shift, db, desc, tile_counter, g->err);
+                st = sort_pass<kHistogram>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m, shift, vn,
+                                           counts, offsets, desc, tile_counter);
             else
-                launch_pass<kWriteKeys>(radix_tiles, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
-                                        shift, db, desc, tile_counter, g->err);
-            PRK_CUDA(cudaGetLastError(), "k_radix_pass launch");
-            ++g->build_launches;
+                st = sort_pass<kWriteKeys>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m, shift, vn,
+                                           counts, offsets, desc, tile_counter);
+            if (st != PR_OK)
+                return st;
+            if (first) {
+                // stop on an invalid col_idx before its destinations are used
+                PRK_TRY(read_err(g, s, &herr));
+                if (herr & kErrColIdx)
+                    return set_error(PR_ERR_INVALID_GRAPH, "col_idx has an entry outside [0, n)");
+            }
         }
     }
 
@@ -1062,30 +1048,25 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         int32_t *okeys = nullptr, *ovals = nullptr;
         PRK_TRY(tmp.alloc((void **)&okeys, (size_t)n * sizeof(int32_t)));
         PRK_TRY(tmp.alloc((void **)&ovals, (size_t)n * sizeof(int32_t)));
-        PRK_CUDA(cudaMemsetAsync(hist, 0, kMaxPasses * kRadixBins * sizeof(unsigned), s), "memset");
         k_order_keys<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, g->deg_out, okeys, ovals);
-        k_digit_hist<<<grid_for(n, kBlock * 16, cap), kBlock, 0, s>>>(okeys, n, 0, 1, hist, g->err);
-        k_digit_base<<<1, kRadixBins, 0, s>>>(hist, 1, dbase);
-        const int64_t otiles = (n + kRadixTile - 1) / kRadixTile;
-        PRK_CUDA(cudaMemsetAsync(desc, 0, (size_t)otiles * kRadixBins * sizeof(unsigned long long), s),
-                 "memset");
-        PRK_CUDA(cudaMemsetAsync(tile_counter, 0, sizeof(unsigned), s), "memset");
-        launch_pass<0u>(otiles, s, okeys, ovals, nullptr, n, nullptr, g->order, nullptr, n, 0, dbase,
-                        desc, tile_counter, g->err);
+        ++g->build_launches;
+        PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, nullptr, n, nullptr, g->order, nullptr, n, 0, 0, counts,
+                              offsets, desc, tile_counter));
         k_invert<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->perm);
-        g->build_launches += 5;
+        ++g->build_launches;
         PRK_CUDA(cudaGetLastError(), "order launch");
     }
-    unsigned h_hist[kRadixBins];
-    PRK_CUDA(cudaMemcpyAsync(h_hist, hist, sizeof(h_hist), cudaMemcpyDeviceToHost, s), "class counts");
+    // class sizes: the scanned counts at the digit boundaries 64, 128, 192, 256
+    // (keys are class * 64 + bucket)
+    int32_t h_cls[4];
+    for (int q = 0; q < 4; ++q)
+        PRK_CUDA(cudaMemcpyAsync(&h_cls[q], offsets + (int64_t)(q + 1) * 64 * order_tiles, sizeof(int32_t),
+                                 cudaMemcpyDeviceToHost, s), "class counts");
     PRK_TRY(check_timeout());
-    int64_t cls[4] = {0, 0, 0, 0};
-    for (int b = 0; b < kRadixBins; ++b)
-        cls[b / 64] += h_hist[b];
-    g->n_c = cls[0];
-    g->n_w = cls[1];
-    g->n_t = cls[2];
-    g->n_z = cls[3];
+    g->n_c = h_cls[0];
+    g->n_w = h_cls[1] - h_cls[0];
+    g->n_t = h_cls[2] - h_cls[1];
+    g->n_z = h_cls[3] - h_cls[2];
 
     // the work CSR in class-major order
     PRK_TRY(launch_scan(LoadOrderDeg{g->in_ptr, g->order}, g->w_ptr, n, desc, tile_counter, g->err,
@@ -1097,11 +1078,11 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
              "work size");
     PRK_TRY(check_timeout());
     g->m_w = h_mw;
-    PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t), s));
 
     // CTA rows (work rows [0, n_c)) -> chunks
-    PRK_TRY(graph_alloc(g, (void **)&g->chunk_first, (size_t)(g->n_c + 1) * sizeof(int32_t)));
-    PRK_TRY(graph_alloc(g, (void **)&g->hub_arrivals, (size_t)(g->n_c + 1) * sizeof(uint32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->chunk_first, (size_t)(g->n_c + 1) * sizeof(int32_t), s));
+    PRK_TRY(graph_alloc(g, (void **)&g->hub_arrivals, (size_t)(g->n_c + 1) * sizeof(uint32_t), s));
     PRK_CUDA(cudaMemsetAsync(g->hub_arrivals, 0, (size_t)(g->n_c + 1) * sizeof(uint32_t), s), "memset");
     PRK_TRY(launch_scan(LoadChunkCount{g->w_ptr}, g->chunk_first, g->n_c, desc, tile_counter, g->err,
                         &g->build_launches, s));
@@ -1110,7 +1091,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
                              cudaMemcpyDeviceToHost, s), "chunk count");
     PRK_TRY(check_timeout());
     g->n_chunks = h_chunks;
-    PRK_TRY(graph_alloc(g, (void **)&g->chunk_row, (size_t)g->n_chunks * sizeof(int32_t)));
+    PRK_TRY(graph_alloc(g, (void **)&g->chunk_row, (size_t)g->n_chunks * sizeof(int32_t), s));
     g->build_launches += (g->n_c > 0);
     if (g->n_c > 0)
         k_fill_chunks<<<grid_for(g->n_c, 1, cap), kBlock, 0, s>>>(g->n_c, g->n_chunks, g->chunk_first,
