@@ -89,8 +89,9 @@ __device__ __forceinline__ T block_sum(T v, T *red)
 }
 
 // The gathered state: slots below `hot` come from the CTA's shared-memory
-// copy of the head of the state vector, the rest from global memory, and a
-// padding entry (kPadSource, negative) contributes 0.
+// copy of the head of the state vector, the rest from L2 (ld.global.cg: a
+// random gather gains nothing from L1, and not allocating there leaves L1 to
+// the loads in flight). A padding entry (kPadSource, negative) contributes 0.
 template <typename T>
 struct Gather {
     const T *__restrict__ s;   // global state (s_old)
@@ -98,7 +99,7 @@ struct Gather {
     int32_t hot;
     __device__ __forceinline__ T operator()(int32_t u) const
     {
-        return u < 0 ? T(0) : u < hot ? h[u] : __ldg(s + u);
+        return u < 0 ? T(0) : u < hot ? h[u] : __ldcg(s + u);
     }
     __device__ __forceinline__ T four(int4 q) const
     {
@@ -154,15 +155,13 @@ __device__ __forceinline__ double from_fixed(unsigned long long f)
 __device__ __forceinline__ float abs_t(float x) { return fabsf(x); }
 __device__ __forceinline__ double abs_t(double x) { return ::fabs(x); }
 
-// The combine for work row i: new rank, new state, L1 and dangling-mass terms.
+// The combine for work row i, given its out-degree and old state: new rank,
+// new state, L1 and dangling-mass terms.
 template <typename T>
-__device__ __forceinline__ void finish_row(int64_t i, T y, const int32_t *__restrict__ w_deg,
-                                           const T *__restrict__ s_old, T *__restrict__ s_new,
-                                           T base, T d, unsigned long long &l1,
-                                           unsigned long long &dm)
+__device__ __forceinline__ void combine_row(int64_t i, T y, int32_t deg, T so, T *__restrict__ s_new,
+                                            T base, T d, unsigned long long &l1,
+                                            unsigned long long &dm)
 {
-    const int32_t deg = w_deg[i];
-    const T so = s_old[i];
     const T x_old = deg ? so * T(deg) : so;
     const T x_new = base + d * y;
     l1 += to_fixed(abs_t(x_new - x_old));
@@ -172,6 +171,122 @@ __device__ __forceinline__ void finish_row(int64_t i, T y, const int32_t *__rest
         __stcs(s_new + i, x_new);
         dm += to_fixed(x_new);
     }
+}
+
+template <typename T>
+__device__ __forceinline__ void finish_row(int64_t i, T y, const int32_t *__restrict__ w_deg,
+                                           const T *__restrict__ s_old, T *__restrict__ s_new,
+                                           T base, T d, unsigned long long &l1,
+                                           unsigned long long &dm)
+{
+    combine_row(i, y, w_deg[i], s_old[i], s_new, base, d, l1, dm);
+}
+
+// Offsets of a block of up to 32 consecutive work rows [r0, r0 + cnt), in
+// 16-byte units: lane j gets row j's start relative to the block's first
+// int4 (rows past cnt get nvec).
+struct RowBlock {
+    int32_t seg0;   // first int4 of the block
+    int32_t nvec;   // int4s in the block
+    int32_t cs;     // this lane's row start, relative to seg0
+};
+
+__device__ __forceinline__ RowBlock load_row_block(const int32_t *__restrict__ w_ptr, int64_t r0, int cnt,
+                                                   int lane)
+{
+    RowBlock b;
+    const int32_t mine = lane < cnt ? w_ptr[r0 + lane] : 0;
+    const int32_t end = w_ptr[r0 + cnt];
+    b.seg0 = __shfl_sync(0xffffffffu, mine, 0) >> 2;
+    b.nvec = (end >> 2) - b.seg0;
+    b.cs = lane < cnt ? (mine >> 2) - b.seg0 : b.nvec;
+    return b;
+}
+
+// Row sum of a thread-class row, lane j owning row j of a block of cnt <= 32
+// consecutive rows. The rows of a block all span len int4s, stored
+// interleaved: int4 k of row j at blk + k * cnt + j, so a warp's loads are
+// coalesced. Up to four int4s (16 gathers) per lane in flight.
+template <typename T>
+__device__ __forceinline__ T lane_row_sum(const int4 *__restrict__ blk, int32_t len, int32_t cnt,
+                                          const Gather<T> &gat)
+{
+    T y = T(0);
+    for (int32_t k = 0; k < len; k += 4) {
+        int4 q[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (k + t < len)
+                q[t] = ld_stream4(blk + (k + t) * cnt);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (k + t < len)
+                y += gat.four(q[t]);
+    }
+    return y;
+}
+
+// Row sums of a block of up to 32 consecutive work rows, each padded to
+// whole int4s, lane j owning row j. The warp streams the block's int4s in
+// coalesced 32-wide steps, U steps of loads (4U gathers per lane) in flight
+// at once, so every lane has work whatever the row lengths. The row of each
+// int4 comes from a bisection over the lanes' row starts, and a segmented
+// scan forms each row's run within the step: the lane holding the run's last
+// int4 hands the run sum to the row's owner. A row may span many steps. The
+// order of every addition is fixed by the layout, so the sums repeat bit for
+// bit.
+template <int U, typename T>
+__device__ __forceinline__ T block_row_sums(const RowBlock &b, int cnt, const int4 *__restrict__ cv,
+                                            const Gather<T> &gat, int lane)
+{
+    int32_t ce = __shfl_down_sync(0xffffffffu, b.cs, 1);
+    if (lane >= cnt - 1)
+        ce = b.nvec;
+    T acc = T(0);
+    for (int32_t p0 = 0; p0 < b.nvec; p0 += 32 * U) {
+        int4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int32_t p = p0 + 32 * u + lane;
+            if (p < b.nvec)
+                q[u] = ld_stream4(cv + b.seg0 + p);
+        }
+        T v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            v[u] = (p0 + 32 * u + lane < b.nvec) ? gat.four(q[u]) : T(0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int32_t ps = p0 + 32 * u;   // warp-uniform
+            if (ps < b.nvec) {
+                const int32_t p = ps + lane;
+                int32_t row = 0, rs = 0;   // largest j < cnt with cs_j <= p, and cs_j
+#pragma unroll
+                for (int step = 16; step >= 1; step >>= 1) {
+                    const int32_t cand = row + step;
+                    const int32_t c_cs = __shfl_sync(0xffffffffu, b.cs, cand & 31);
+                    if (cand < cnt && c_cs <= p) {
+                        row = cand;
+                        rs = c_cs;
+                    }
+                }
+                // lanes [lo, lane] of this step hold int4s of this lane's row
+                const int lo = max(rs - ps, 0);
+                T x = v[u];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const T t = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane - o >= lo)
+                        x += t;
+                }
+                const int32_t last = min(ce, ps + 32) - 1;   // row's last int4 in this step
+                const T got = __shfl_sync(0xffffffffu, x, (last - ps) & 31);
+                if (lane < cnt && last >= max(b.cs, ps))
+                    acc += got;
+            }
+        }
+    }
+    return acc;
 }
 
 template <typename T>
@@ -277,107 +392,68 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         }
     }
 
-    // warp class: one warp per row, 33..1024 in-edges (16-byte aligned,
-    // whole int4s). Each warp owns one contiguous range of these rows, cut so
-    // that every warp has about the same edges (w_split). It reads the
-    // offsets of 32 rows in one coalesced load, walks them four rows at a time
-    // so that each lane has up to 16 gathers in flight, and combines row q in
-    // lane q.
+    // warp class (33..1024 in-edges) and thread class (1..32), in blocks of
+    // 32 consecutive rows. Warp-class rows: each warp owns one contiguous
+    // range of rows, cut so that every warp has about the same edges
+    // (w_split), and streams each block's int4s (block_row_sums).
+    // Thread-class rows: the warps of the grid sweep the blocks round-robin,
+    // one row per lane, the block stored interleaved (lane_row_sum). The old state and out-degree of a
+    // block's rows are loaded before its gathers, and the next block's
+    // offsets while they are in flight.
     {
+        const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
         const int64_t r_begin = a.w_split[gw], r_end = a.w_split[gw + 1];
-        const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
-        for (int64_t r0 = r_begin; r0 < r_end; r0 += 32) {
-            const int cnt = (int)min((int64_t)32, r_end - r0);
-            int32_t rb = 0, re = 0;
-            if (lane < cnt) {
-                rb = a.w_ptr[r0 + lane];
-                re = a.w_ptr[r0 + lane + 1];
+        if (r_begin < r_end) {
+            RowBlock nb = load_row_block(a.w_ptr, r_begin, (int)min((int64_t)32, r_end - r_begin), lane);
+            for (int64_t r0 = r_begin; r0 < r_end; r0 += 32) {
+                const int cnt = (int)min((int64_t)32, r_end - r0);
+                const RowBlock b = nb;
+                int32_t deg = 0;
+                T so = T(0);
+                if (lane < cnt) {
+                    deg = a.w_deg[r0 + lane];
+                    so = s_old[r0 + lane];
+                }
+                const int64_t r1 = r0 + 32;
+                if (r1 < r_end)
+                    nb = load_row_block(a.w_ptr, r1, (int)min((int64_t)32, r_end - r1), lane);
+                const T y = block_row_sums<4>(b, cnt, cv, gat, lane);
+                if (lane < cnt)
+                    combine_row(r0 + lane, y, deg, so, s_new, base, d, l1, dm);
             }
-            T mine = T(0);
-            for (int q0 = 0; q0 < cnt; q0 += 4) {
-                int32_t b4[4], l4[4];
-                int32_t lmax = 0;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int32_t b = __shfl_sync(0xffffffffu, rb, (q0 + t) & 31);
-                    const int32_t e = __shfl_sync(0xffffffffu, re, (q0 + t) & 31);
-                    b4[t] = b >> 2;
-                    l4[t] = (q0 + t < cnt) ? ((e - b) >> 2) : 0;
-                    lmax = max(lmax, l4[t]);
-                }
-                T y[4] = {T(0), T(0), T(0), T(0)};
-                for (int32_t k = lane; k < lmax; k += 32) {
-                    int4 v[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (k < l4[t])
-                            v[t] = ld_stream4(cv + b4[t] + k);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (k < l4[t])
-                            y[t] += gat.four(v[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const T sum = warp_sum(y[t]);
-                    if (lane == q0 + t)
-                        mine = sum;
-                }
-            }
-            if (lane < cnt)
-                finish_row(r0 + lane, mine, a.w_deg, s_old, s_new, base, d, l1, dm);
         }
-    }
 
-    // thread class: one thread per row, 1..32 in-edges, padded to whole
-    // int4s. The warps of the grid sweep these rows together in blocks of 32;
-    // lane j owns row j of a block. The block's rows are contiguous in the
-    // work CSR, so the warp streams their int4s with coalesced loads (32 per
-    // step), finds the row of each int4 by bisection over the lanes' row
-    // starts, and forms the row sums with a segmented scan: the lane holding a
-    // row's last int4 of the step hands the run's sum to the row's owner. An
-    // int4 never straddles two rows (every row is padded), and every sum is
-    // formed in a fixed order.
-    {
         const int64_t t_begin = a.n_c + a.n_w, t_end = t_begin + a.n_t;
-        const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
-        for (int64_t r0 = t_begin + gw * 32; r0 < t_end; r0 += G * kWarps * 32) {
-            const int cnt = (int)min((int64_t)32, t_end - r0);
-            const int32_t seg0 = a.w_ptr[r0] >> 2;
-            const int32_t nvec = (a.w_ptr[r0 + cnt] >> 2) - seg0;
-            // int4 range [cs, ce) of row `lane`, relative to the segment start
-            const int32_t cs = (lane < cnt) ? (a.w_ptr[r0 + lane] >> 2) - seg0 : nvec;
-            int32_t ce = __shfl_down_sync(0xffffffffu, cs, 1);
-            if (lane >= cnt - 1)
-                ce = nvec;
-            T acc = T(0);
-            for (int32_t p0 = 0; p0 < nvec; p0 += 32) {
-                const int32_t p = p0 + lane;
-                T v = T(0);
-                if (p < nvec)
-                    v = gat.four(ld_stream4(cv + seg0 + p));
-                int32_t row = 0;   // largest j < cnt with cs_j <= p
-#pragma unroll
-                for (int step = 16; step >= 1; step >>= 1) {
-                    const int32_t cand = row + step;
-                    const int32_t c_cs = __shfl_sync(0xffffffffu, cs, cand & 31);
-                    if (cand < cnt && c_cs <= p)
-                        row = cand;
+        const int64_t t_stride = G * kWarps * 32;
+        int64_t r0 = t_begin + gw * 32;
+        if (r0 < t_end) {
+            int32_t nb = r0 + lane <= t_end ? a.w_ptr[r0 + lane] : 0;
+            int32_t ne = __shfl_down_sync(0xffffffffu, nb, 1);
+            if (lane == 31 && r0 + 32 <= t_end)
+                ne = a.w_ptr[r0 + 32];
+            for (; r0 < t_end; r0 += t_stride) {
+                const int64_t i = r0 + lane;
+                const bool act = i < t_end;
+                const int cnt = (int)min((int64_t)32, t_end - r0);
+                const int32_t blk4 = __shfl_sync(0xffffffffu, nb, 0) >> 2;   // the block's first int4
+                const int32_t len = act ? (ne - nb) >> 2 : 0;
+                int32_t deg = 0;
+                T so = T(0);
+                if (act) {
+                    deg = a.w_deg[i];
+                    so = s_old[i];
                 }
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const T t = __shfl_up_sync(0xffffffffu, v, o);
-                    const int32_t rr = __shfl_up_sync(0xffffffffu, row, o);
-                    if (lane >= o && rr == row)
-                        v += t;
+                const int64_t r1 = r0 + t_stride;
+                if (r1 < t_end) {
+                    nb = r1 + lane <= t_end ? a.w_ptr[r1 + lane] : 0;
+                    ne = __shfl_down_sync(0xffffffffu, nb, 1);
+                    if (lane == 31 && r1 + 32 <= t_end)
+                        ne = a.w_ptr[r1 + 32];
                 }
-                const int32_t last = min(ce, p0 + 32) - 1;   // row's last int4 in this step
-                const T got = __shfl_sync(0xffffffffu, v, (last - p0) & 31);
-                if (lane < cnt && last >= max(cs, p0))
-                    acc += got;
+                const T y = lane_row_sum(cv + blk4 + lane, len, cnt, gat);
+                if (act)
+                    combine_row(i, y, deg, so, s_new, base, d, l1, dm);
             }
-            if (lane < cnt)
-                finish_row(r0 + lane, acc, a.w_deg, s_old, s_new, base, d, l1, dm);
         }
     }
 

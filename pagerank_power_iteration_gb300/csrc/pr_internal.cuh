@@ -27,7 +27,9 @@ constexpr int kHotBytes = 160 * 1024;   // shared-memory copy of the state's hea
 // Per-row cost, in edges, used to balance warp-class rows over the warps of
 // the update kernel (offset loads, reduction, combine).
 constexpr int kWarpRowCost = 32;
-// Work-CSR entry that pads a row to whole 16-byte loads; it gathers 0.
+// Work-CSR entry that pads a row to whole 16-byte loads; it gathers 0. (A
+// pad pointing at a zero slot of the state instead makes every pad of every
+// SM read one L2 line, a hot spot that was measured to cost 15 %.)
 constexpr int32_t kPadSource = -1;
 
 enum RowClass : int { kClassZero = 0, kClassThread = 1, kClassWarp = 2, kClassCta = 3 };

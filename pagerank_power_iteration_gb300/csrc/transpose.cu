@@ -521,11 +521,18 @@ __device__ __forceinline__ int32_t padded_degree(int32_t deg)
     return (deg + 3) & ~3;
 }
 
+// Padded length of work row i. Thread-class rows (work rows [t_begin,
+// t_end)) are stored in interleaved blocks of 32 and take the padded length
+// of their block's first row, the longest of the block (the work order sorts
+// them by length, longest first), so every row of a block has one length.
 struct LoadOrderDeg {
     const int32_t *in_ptr;
     const int32_t *order;
+    int64_t t_begin, t_end;
     __device__ int32_t operator()(int64_t i) const
     {
+        if (i >= t_begin && i < t_end)
+            i = t_begin + ((i - t_begin) & ~(int64_t)31);
         const int32_t v = order[i];
         return padded_degree(in_ptr[v + 1] - in_ptr[v]);
     }
@@ -632,16 +639,23 @@ __device__ __forceinline__ int degree_bucket(int32_t deg)
     return min(63, 2 * b + half);
 }
 
-// Sort key of the work order: class slot, then out-degree bucket, largest
-// first (the most gathered vertices lead), ties by vertex id (the sort is
-// stable over vals = ids).
+// Sort key of the work order (8 bits): the class slot, then, within the
+// class, out-degree bucket, largest first (the most gathered vertices lead).
+// Thread-class rows are keyed by their length in int4s first (longest first,
+// 8 lengths) and then by a coarse out-degree bucket (8 levels), so that the
+// 32 rows one warp takes together mostly have the same length. Ties go by
+// vertex id (the sort is stable over vals = ids).
 __global__ void k_order_keys(int64_t n, const int32_t *__restrict__ in_ptr,
                              const int32_t *__restrict__ deg_out, int32_t *__restrict__ keys,
                              int32_t *__restrict__ vals)
 {
     for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n;
          v += (int64_t)gridDim.x * blockDim.x) {
-        keys[v] = class_slot(in_ptr[v + 1] - in_ptr[v]) * 64 + (63 - degree_bucket(deg_out[v]));
+        const int32_t indeg = in_ptr[v + 1] - in_ptr[v];
+        const int slot = class_slot(indeg);
+        const int ob = degree_bucket(deg_out[v]);
+        const int sub = slot == 2 ? (8 - ((indeg + 3) >> 2)) * 8 + (7 - min(7, ob >> 2)) : 63 - ob;
+        keys[v] = slot * 64 + sub;
         vals[v] = (int32_t)v;
     }
 }
@@ -661,6 +675,13 @@ __global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *
 // are copied in their kChunkEdges chunks, one warp per chunk; warp-class rows
 // by one warp each; thread-class rows by one thread each. Rows without
 // in-edges have nothing to copy.
+//
+// Thread-class rows are interleaved by blocks of 32 consecutive work rows
+// (the last block may hold fewer, cnt): all rows of a block have the same
+// padded length L int4s (see LoadOrderDeg), the block occupies the int4s
+// [w_ptr[r0] / 4, w_ptr[r0] / 4 + cnt * L), and int4 k of the block's row j
+// sits at w_ptr[r0] / 4 + k * cnt + j, so that the lanes of a warp, one row
+// each, read consecutive int4s.
 __global__ void __launch_bounds__(kBlock)
 k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t rows_end,
           const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_first,
@@ -692,9 +713,13 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
     for (int64_t i = wide_end + gtid; i < rows_end; i += nthreads) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
-        const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
+        const int64_t r0 = wide_end + ((i - wide_end) & ~(int64_t)31);
+        const int64_t cnt = min((int64_t)32, rows_end - r0);
+        const int64_t j = i - r0;
+        const int64_t blk = w_ptr[r0];
+        const int32_t len = w_ptr[i + 1] - w_ptr[i];
         for (int32_t k = 0; k < len; ++k)
-            w_col[dst + k] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
+            w_col[blk + 4 * ((k >> 2) * cnt + j) + (k & 3)] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
     }
 }
 
@@ -1069,7 +1094,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     g->n_z = h_cls[3] - h_cls[2];
 
     // the work CSR in class-major order
-    PRK_TRY(launch_scan(LoadOrderDeg{g->in_ptr, g->order}, g->w_ptr, n, desc, tile_counter, g->err,
+    PRK_TRY(launch_scan(LoadOrderDeg{g->in_ptr, g->order, g->n_c + g->n_w, g->n_c + g->n_w + g->n_t},
+                        g->w_ptr, n, desc, tile_counter, g->err,
                         &g->build_launches, s));
     k_permute_deg<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->deg_out, g->w_deg);
     ++g->build_launches;
