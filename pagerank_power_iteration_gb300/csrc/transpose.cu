@@ -224,15 +224,22 @@ constexpr int kRadixBins = 1 << kRadixBits;
 constexpr int kRadixItems = 8;
 constexpr int kRadixTile = kBlock * kRadixItems;
 
-// Upsweep of one counting-sort pass: the 256 digit counts of every tile,
-// written digit-major (counts[d * tiles + t]), so that one exclusive scan of
-// the whole array gives every (digit, tile) its output position. With n > 0
-// every key is also checked against [0, n); a bad key is still counted, so
-// the downsweep's positions stay a permutation of [0, count) and the build
-// stops on the error flag before any later step reads them.
+// Tiles [tile_lo(c), tile_lo(c + 1)) of a pass belong to CTA c of `ctas`:
+// contiguous ranges, so that a CTA's output for each digit is one run.
+__device__ __forceinline__ int64_t tile_lo(int64_t c, int64_t tiles, int64_t ctas)
+{
+    return tiles * c / ctas;
+}
+
+// Upsweep of one counting-sort pass: the 256 digit counts of each CTA's tile
+// range, written digit-major (counts[d * ctas + c]), so that one exclusive
+// scan of the whole array gives every (digit, CTA) its output position. With
+// n > 0 every key is also checked against [0, n); a bad key is still
+// counted, so the downsweep's positions stay a permutation of [0, count) and
+// the build stops on the error flag before any later step reads them.
 __global__ void __launch_bounds__(kBlock)
 k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int shift,
-                int32_t *__restrict__ counts, int64_t tiles, unsigned *err)
+                int32_t *__restrict__ counts, int64_t tiles, int64_t ctas, unsigned *err)
 {
     constexpr int kWarps = kBlock / 32;
     __shared__ unsigned s_h[kWarps][kRadixBins];
@@ -240,33 +247,40 @@ k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int 
     for (int w = 0; w < kWarps; ++w)
         s_h[w][tid] = 0;
     __syncthreads();
-    const int64_t tile = blockIdx.x;
-    const int64_t begin = tile * kRadixTile;
+    const int64_t c = blockIdx.x;
+    const int64_t i_end = min(count, tile_lo(c + 1, tiles, ctas) * kRadixTile);
     bool bad = false;
+    for (int64_t b = tile_lo(c, tiles, ctas) * kRadixTile; b < i_end; b += kRadixTile) {
+        int32_t v[kRadixItems];
 #pragma unroll
-    for (int k = 0; k < kRadixItems; ++k) {
-        const int64_t i = begin + (int64_t)k * kBlock + tid;
-        if (i < count) {
-            const int32_t v = keys[i];
-            bad |= n > 0 && (v < 0 || (int64_t)v >= n);
-            atomicAdd(&s_h[warp][((unsigned)v >> shift) & (kRadixBins - 1)], 1u);
+        for (int k = 0; k < kRadixItems; ++k) {
+            const int64_t i = b + (int64_t)k * kBlock + tid;
+            v[k] = i < i_end ? keys[i] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kRadixItems; ++k) {
+            if (b + (int64_t)k * kBlock + tid < i_end) {
+                bad |= n > 0 && (v[k] < 0 || (int64_t)v[k] >= n);
+                atomicAdd(&s_h[warp][((unsigned)v[k] >> shift) & (kRadixBins - 1)], 1u);
+            }
         }
     }
     if (bad)
         atomicOr(err, kErrColIdx);
     __syncthreads();
-    unsigned c = 0;
+    unsigned t = 0;
     for (int w = 0; w < kWarps; ++w)
-        c += s_h[w][tid];
-    counts[(int64_t)tid * tiles + tile] = (int32_t)c;
+        t += s_h[w][tid];
+    counts[(int64_t)tid * ctas + c] = (int32_t)t;
 }
 
 // ---------------------------------------------------------------- step 3 --
 
 // Downsweep of one stable counting-sort pass over digit (key >> shift) & 255.
-// `offsets` is the exclusive scan of the upsweep's digit-major tile counts:
-// offsets[d * tiles + t] is where tile t's keys of digit d go, so tiles are
-// independent and none waits for another.
+// CTA c sorts its tile range in order. `offsets` is the exclusive scan of the
+// upsweep's digit-major counts: offsets[d * ctas + c] is where CTA c's keys of
+// digit d start, and the CTA keeps each digit's running position in shared
+// memory from tile to tile, so no CTA waits for another.
 //
 // Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
 // walks them in 32-key rounds, so "earlier round, then lower lane" is input
@@ -275,7 +289,9 @@ k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int 
 // Per-warp counts are then scanned across warps (and across digits for the
 // tile-local order) and the tile is staged in shared memory in (digit,
 // input) order. The write-out walks the staged tile linearly, so a warp
-// stores consecutive addresses of one bucket.
+// stores consecutive addresses of one bucket, and a CTA's stores of one digit
+// continue where its previous tile's ended. The next tile's keys are loaded
+// while the current one is written out.
 //
 // kFlags:
 //   kSrcRows   the values are the edges' sources: the input is the out-edge
@@ -292,15 +308,16 @@ enum : unsigned { kSrcRows = 1u, kWriteKeys = 2u, kHistogram = 4u };
 
 __device__ __forceinline__ int spad(int i) { return i + (i >> 5); }   // bank-conflict padding
 
-// Block-wide inclusive max-scan of `count` shared entries, kRadixItems
-// consecutive entries per thread.
-__device__ __forceinline__ void block_max_scan(int32_t *a, int count, int32_t *s_wmax)
+// Block-wide inclusive max-scan of the kRadixTile entries of `a` (16-byte
+// aligned, unpadded), kRadixItems = 8 consecutive entries per thread, read
+// and written as two int4s.
+__device__ __forceinline__ void block_max_scan(int32_t *a, int32_t *s_wmax)
 {
+    static_assert(kRadixItems == 8, "two int4s per thread");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int j0 = tid * kRadixItems;
-    int32_t run = INT32_MIN;
-    for (int j = j0; j < j0 + kRadixItems && j < count; ++j)
-        run = max(run, a[spad(j)]);
+    int4 *a4 = reinterpret_cast<int4 *>(a) + 2 * tid;
+    int4 q0 = a4[0], q1 = a4[1];
+    const int32_t run = max(max(max(q0.x, q0.y), max(q0.z, q0.w)), max(max(q1.x, q1.y), max(q1.z, q1.w)));
     int32_t incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -317,10 +334,16 @@ __device__ __forceinline__ void block_max_scan(int32_t *a, int count, int32_t *s
     const int32_t up = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane > 0)
         carry = max(carry, up);
-    for (int j = j0; j < j0 + kRadixItems && j < count; ++j) {
-        carry = max(carry, a[spad(j)]);
-        a[spad(j)] = carry;
-    }
+    q0.x = carry = max(carry, q0.x);
+    q0.y = carry = max(carry, q0.y);
+    q0.z = carry = max(carry, q0.z);
+    q0.w = carry = max(carry, q0.w);
+    q1.x = carry = max(carry, q1.x);
+    q1.y = carry = max(carry, q1.y);
+    q1.z = carry = max(carry, q1.z);
+    q1.w = carry = max(carry, q1.w);
+    a4[0] = q0;
+    a4[1] = q1;
     __syncthreads();
 }
 
@@ -329,165 +352,184 @@ __global__ void __launch_bounds__(kBlock, 4)
 k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ vals_in,
              const int64_t *__restrict__ row_ptr, int64_t n, int32_t *__restrict__ keys_out,
              int32_t *__restrict__ vals_out, int32_t *__restrict__ in_deg, int64_t count,
-             int shift, const int32_t *__restrict__ offsets, int64_t tiles)
+             int shift, const int32_t *__restrict__ offsets, int64_t tiles, int64_t ctas)
 {
     constexpr int kWarps = kBlock / 32;
     constexpr int kWarpSpan = 32 * kRadixItems;
     constexpr int kPadTile = kRadixTile + kRadixTile / 32;
     __shared__ unsigned s_wh[kWarps][kRadixBins];   // per-warp counts, then offsets
     __shared__ unsigned s_start[kRadixBins];        // tile-local start of each digit
-    __shared__ unsigned s_base[kRadixBins];         // global start of this tile's digit run
+    __shared__ unsigned s_run[kRadixBins];          // next output position of each digit
+    __shared__ unsigned s_delta[kRadixBins];        // output position - staged position, per digit
     __shared__ unsigned s_wsum[kWarps];
     __shared__ int32_t s_wmax[kWarps];
-    __shared__ int32_t s_key[kPadTile];
-    __shared__ int32_t s_val[kPadTile];             // also the row map of kSrcRows
+    __shared__ __align__(16) int32_t s_key[kPadTile];   // also the row map of kSrcRows (unpadded)
+    __shared__ int32_t s_val[kPadTile];
     __shared__ int64_t s_row_lo, s_row_hi;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int w = 0; w < kWarps; ++w)
-        s_wh[w][tid] = 0;
-    const int64_t tile = blockIdx.x;
-    // where this tile's run of each digit starts in the output
-    s_base[tid] = (unsigned)offsets[(int64_t)tid * tiles + tile];
-    __syncthreads();
-    const int64_t tile_begin = tile * kRadixTile;
-    const int tile_count = (int)min((int64_t)kRadixTile, count - tile_begin);
-    const int64_t base = tile_begin + (int64_t)warp * kWarpSpan;
-
-    if (kFlags & kSrcRows) {
-        // row of every position of the tile: mark row starts, then max-scan.
-        // tile_rows (vals_in here) holds the row of each tile's first
-        // position, so [row of first, row of next tile's first] covers the tile.
-        if (tid == 0) {
-            s_row_lo = vals_in[tile];
-            s_row_hi = vals_in[tile + 1];
-        }
-        for (int j = tid; j < tile_count; j += kBlock)
-            s_val[spad(j)] = INT32_MIN;
-        __syncthreads();
-        const int64_t rlo = s_row_lo, rhi = s_row_hi;
-        if (tid == 0)
-            s_val[spad(0)] = (int32_t)rlo;
-        __syncthreads();
-        for (int64_t r = rlo + 1 + tid; r <= rhi; r += kBlock) {
-            const int64_t p = row_ptr[r] - tile_begin;   // rows starting past the tile are skipped
-            if (p > 0 && p < tile_count)
-                atomicMax(&s_val[spad((int)p)], (int32_t)r);
-        }
-        __syncthreads();
-        block_max_scan(s_val, tile_count, s_wmax);
-    }
+    const int64_t c = blockIdx.x;
+    const int64_t t_first = tile_lo(c, tiles, ctas), t_last = tile_lo(c + 1, tiles, ctas);
+    s_run[tid] = (unsigned)offsets[(int64_t)tid * ctas + c];
 
     int32_t key[kRadixItems], val[kRadixItems];
     unsigned rank[kRadixItems];
+    // keys (and values) of tile t into registers
+    auto load_tile = [&](int64_t t) {
+        const int64_t base = t * kRadixTile + (int64_t)warp * kWarpSpan;
 #pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
-        const int64_t i = base + r * 32 + lane;
-        const bool ok = i < count;
-        key[r] = ok ? keys_in[i] : 0;
-        if (kFlags & kSrcRows)
-            val[r] = ok ? s_val[spad((int)(i - tile_begin))] : 0;
-        else
-            val[r] = ok ? vals_in[i] : 0;
-    }
-    if (kFlags & kSrcRows)
-        __syncthreads();   // s_val is reused for staging below
-
-    const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
-        const bool ok = base + r * 32 + lane < count;
-        const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
-        const unsigned peers = __match_any_sync(0xffffffffu, dig);
-        const unsigned before = ok ? s_wh[warp][dig] : 0u;
-        __syncwarp();
-        rank[r] = before + __popc(peers & below);
-        if (ok && (peers >> lane) == 1u)   // highest lane of the group
-            s_wh[warp][dig] = before + __popc(peers);
-        __syncwarp();
-    }
-    __syncthreads();
-
-    // thread tid owns digit tid: exclusive offsets of the warps, and the
-    // tile's count
-    unsigned tot = 0;
-    for (int w = 0; w < kWarps; ++w) {
-        const unsigned c = s_wh[w][tid];
-        s_wh[w][tid] = tot;
-        tot += c;
-    }
-
-    // tile-local start of each digit (exclusive scan over the 256 digits)
-    const unsigned incl = warp_incl_scan(tot, lane);
-    if (lane == 31)
-        s_wsum[warp] = incl;
-    __syncthreads();
-    unsigned woff = 0;
-    for (int w = 0; w < warp; ++w)
-        woff += s_wsum[w];
-    s_start[tid] = woff + incl - tot;
-    __syncthreads();
-
-    // stage the tile in (digit, input) order
-#pragma unroll
-    for (int r = 0; r < kRadixItems; ++r) {
-        if (base + r * 32 + lane < count) {
-            const unsigned dig = ((unsigned)key[r] >> shift) & (kRadixBins - 1);
-            const int lp = (int)(s_start[dig] + s_wh[warp][dig] + rank[r]);
-            s_key[spad(lp)] = key[r];
-            s_val[spad(lp)] = val[r];
+        for (int r = 0; r < kRadixItems; ++r) {
+            const int64_t i = base + r * 32 + lane;
+            const bool ok = i < count;
+            key[r] = ok ? keys_in[i] : 0;
+            if (!(kFlags & kSrcRows))
+                val[r] = ok ? vals_in[i] : 0;
         }
-    }
+    };
+    if (t_first < t_last)
+        load_tile(t_first);
 
-    __syncthreads();
+    for (int64_t tile = t_first; tile < t_last; ++tile) {
+        __syncthreads();   // the previous tile's shared-memory reads are done
+        for (int w = 0; w < kWarps; ++w)
+            s_wh[w][tid] = 0;
+        const int64_t tile_begin = tile * kRadixTile;
+        const int tile_count = (int)min((int64_t)kRadixTile, count - tile_begin);
+        const int64_t base = tile_begin + (int64_t)warp * kWarpSpan;
 
-    // write-out: consecutive staged entries of one digit go to consecutive addresses
+        if (kFlags & kSrcRows) {
+            // row of every position of the tile: mark row starts, then max-scan.
+            // tile_rows (vals_in here) holds the row of each tile's first
+            // position, so [row of first, row of next tile's first] covers the tile.
+            int32_t *rmap = s_key;
+            if (tid == 0) {
+                s_row_lo = vals_in[tile];
+                s_row_hi = vals_in[tile + 1];
+            }
+            const int4 none = make_int4(INT32_MIN, INT32_MIN, INT32_MIN, INT32_MIN);
+            reinterpret_cast<int4 *>(rmap)[2 * tid] = none;
+            reinterpret_cast<int4 *>(rmap)[2 * tid + 1] = none;
+            __syncthreads();
+            const int64_t rlo = s_row_lo, rhi = s_row_hi;
+            if (tid == 0)
+                rmap[0] = (int32_t)rlo;
+            __syncthreads();
+            for (int64_t r = rlo + 1 + tid; r <= rhi; r += kBlock) {
+                const int64_t p = row_ptr[r] - tile_begin;   // rows starting past the tile are skipped
+                if (p > 0 && p < tile_count)
+                    atomicMax(&rmap[(int)p], (int32_t)r);
+            }
+            __syncthreads();
+            block_max_scan(rmap, s_wmax);
 #pragma unroll
-    for (int k = 0; k < kRadixItems; ++k) {
-        const int i = k * kBlock + tid;
-        if (i < tile_count) {
-            const int32_t kv = s_key[spad(i)];
-            const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
-            const int64_t pos = (int64_t)s_base[dig] + (i - (int)s_start[dig]);
-            if (pos < 0 || pos >= count)   // only reachable if the offsets scan failed
-                continue;
-            vals_out[pos] = s_val[spad(i)];
-            if (kFlags & kWriteKeys)
-                keys_out[pos] = kv;
+            for (int r = 0; r < kRadixItems; ++r)
+                val[r] = rmap[warp * kWarpSpan + r * 32 + lane];   // past the tile: never staged
         }
-    }
+        __syncthreads();   // s_wh cleared; the row map read before staging reuses s_key
 
-    if (kFlags & kHistogram) {
-        // thread t owns staged entries [t*ITEMS, (t+1)*ITEMS); each run of
-        // equal keys adds its length once, at its last entry. The head of
-        // the run an entry belongs to comes from a max-scan of run heads.
-        const int j0 = tid * kRadixItems;
-        int head_local = -1;
-        for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j)
-            if (j == 0 || s_key[spad(j)] != s_key[spad(j - 1)])
-                head_local = j;
-        int carry = head_local;
+        const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, carry, o);
-            if (lane >= o)
-                carry = max(carry, t);
+        for (int r = 0; r < kRadixItems; ++r) {
+            const bool ok = base + r * 32 + lane < count;
+            const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
+            const unsigned peers = __match_any_sync(0xffffffffu, dig);
+            const unsigned before = ok ? s_wh[warp][dig] : 0u;
+            __syncwarp();
+            rank[r] = before + __popc(peers & below);
+            if (ok && (peers >> lane) == 1u)   // highest lane of the group
+                s_wh[warp][dig] = before + __popc(peers);
+            __syncwarp();
         }
-        if (lane == 31)
-            s_wmax[warp] = carry;
         __syncthreads();
-        int head = -1;
+
+        // thread tid owns digit tid: exclusive offsets of the warps, the
+        // tile's count, and the digit's output start for this tile
+        unsigned tot = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const unsigned cnt = s_wh[w][tid];
+            s_wh[w][tid] = tot;
+            tot += cnt;
+        }
+        // tile-local start of each digit (exclusive scan over the 256 digits)
+        const unsigned incl = warp_incl_scan(tot, lane);
+        if (lane == 31)
+            s_wsum[warp] = incl;
+        __syncthreads();
+        unsigned woff = 0;
         for (int w = 0; w < warp; ++w)
-            head = max(head, s_wmax[w]);
-        const int up = __shfl_up_sync(0xffffffffu, carry, 1);
-        if (lane > 0)
-            head = max(head, up);   // last run head before this thread's entries
-        for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j) {
-            const int32_t kv = s_key[spad(j)];
-            if (j == 0 || kv != s_key[spad(j - 1)])
-                head = j;
-            if ((j == tile_count - 1 || s_key[spad(j + 1)] != kv) && kv >= 0 && (int64_t)kv < n)
-                atomicAdd(&in_deg[kv], j - head + 1);
+            woff += s_wsum[w];
+        const unsigned start = woff + incl - tot;
+        s_start[tid] = start;
+        // staged position j of digit tid goes to s_run + (j - start); positions
+        // are below count <= 2^31 - 1, so unsigned 32-bit arithmetic is exact
+        s_delta[tid] = s_run[tid] - start;
+        s_run[tid] += tot;
+        __syncthreads();
+
+        // stage the tile in (digit, input) order
+#pragma unroll
+        for (int r = 0; r < kRadixItems; ++r) {
+            if (base + r * 32 + lane < count) {
+                const unsigned dig = ((unsigned)key[r] >> shift) & (kRadixBins - 1);
+                const int lp = (int)(s_start[dig] + s_wh[warp][dig] + rank[r]);
+                s_key[spad(lp)] = key[r];
+                s_val[spad(lp)] = val[r];
+            }
+        }
+        __syncthreads();
+
+        // the next tile's loads overlap this tile's write-out
+        if (tile + 1 < t_last)
+            load_tile(tile + 1);
+
+        // write-out: consecutive staged entries of one digit go to consecutive addresses
+#pragma unroll
+        for (int k = 0; k < kRadixItems; ++k) {
+            const int i = k * kBlock + tid;
+            if (i < tile_count) {
+                const int32_t kv = s_key[spad(i)];
+                const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
+                const unsigned pos = s_delta[dig] + (unsigned)i;
+                if ((int64_t)pos >= count)   // only reachable if the offsets scan failed
+                    continue;
+                vals_out[pos] = s_val[spad(i)];
+                if (kFlags & kWriteKeys)
+                    keys_out[pos] = kv;
+            }
+        }
+
+        if (kFlags & kHistogram) {
+            // thread t owns staged entries [t*ITEMS, (t+1)*ITEMS); each run of
+            // equal keys adds its length once, at its last entry. The head of
+            // the run an entry belongs to comes from a max-scan of run heads.
+            const int j0 = tid * kRadixItems;
+            int head_local = -1;
+            for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j)
+                if (j == 0 || s_key[spad(j)] != s_key[spad(j - 1)])
+                    head_local = j;
+            int carry = head_local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, carry, o);
+                if (lane >= o)
+                    carry = max(carry, t);
+            }
+            if (lane == 31)
+                s_wmax[warp] = carry;
+            __syncthreads();
+            int head = -1;
+            for (int w = 0; w < warp; ++w)
+                head = max(head, s_wmax[w]);
+            const int up = __shfl_up_sync(0xffffffffu, carry, 1);
+            if (lane > 0)
+                head = max(head, up);   // last run head before this thread's entries
+            for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j) {
+                const int32_t kv = s_key[spad(j)];
+                if (j == 0 || kv != s_key[spad(j - 1)])
+                    head = j;
+                if ((j == tile_count - 1 || s_key[spad(j + 1)] != kv) && kv >= 0 && (int64_t)kv < n)
+                    atomicAdd(&in_deg[kv], j - head + 1);
+            }
         }
     }
 }
@@ -820,8 +862,16 @@ pr_status read_err(pr_graph *g, cudaStream_t s, unsigned *out)
     return e == cudaSuccess ? PR_OK : cuda_status(e, "reading the error word");
 }
 
-// One counting-sort pass: upsweep (digit counts per tile), one exclusive
-// scan of the digit-major counts, downsweep (rank and scatter).
+// CTAs of a counting-sort pass over `tiles` tiles: four per SM (the
+// downsweep's occupancy), each with a contiguous tile range.
+int64_t sort_ctas(const pr_graph *g, int64_t tiles)
+{
+    const int64_t want = (int64_t)g->num_sms * 4;
+    return tiles < want ? tiles : want;
+}
+
+// One counting-sort pass: upsweep (digit counts per CTA range), one
+// exclusive scan of the digit-major counts, downsweep (rank and scatter).
 template <unsigned kFlags>
 pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32_t *vin,
                     const int64_t *row_ptr, int64_t n, int32_t *kout, int32_t *vout, int32_t *in_deg,
@@ -829,17 +879,19 @@ pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32
                     unsigned long long *desc, unsigned *counter)
 {
     const int64_t tiles = (count + kRadixTile - 1) / kRadixTile;
-    k_radix_upsweep<<<(unsigned)tiles, kBlock, 0, s>>>(kin, count, validate_n, shift, counts, tiles, g->err);
+    const int64_t ctas = sort_ctas(g, tiles);
+    k_radix_upsweep<<<(unsigned)ctas, kBlock, 0, s>>>(kin, count, validate_n, shift, counts, tiles, ctas,
+                                                      g->err);
     ++g->build_launches;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_status(e, "k_radix_upsweep launch");
-    pr_status st = launch_scan(LoadCount{counts}, offsets, tiles * kRadixBins, desc, counter, g->err,
+    pr_status st = launch_scan(LoadCount{counts}, offsets, ctas * kRadixBins, desc, counter, g->err,
                                &g->build_launches, s);
     if (st != PR_OK)
         return st;
-    k_radix_pass<kFlags><<<(unsigned)tiles, kBlock, 0, s>>>(kin, vin, row_ptr, n, kout, vout, in_deg,
-                                                           count, shift, offsets, tiles);
+    k_radix_pass<kFlags><<<(unsigned)ctas, kBlock, 0, s>>>(kin, vin, row_ptr, n, kout, vout, in_deg, count,
+                                                          shift, offsets, tiles, ctas);
     ++g->build_launches;
     e = cudaGetLastError();
     return e == cudaSuccess ? PR_OK : cuda_status(e, "k_radix_pass launch");
@@ -984,7 +1036,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     const int64_t radix_tiles = (m + kRadixTile - 1) / kRadixTile;
     const int64_t order_tiles = (n + kRadixTile - 1) / kRadixTile;
     const int64_t max_tiles = radix_tiles > order_tiles ? radix_tiles : order_tiles;
-    const int64_t count_words = max_tiles * kRadixBins;
+    const int64_t count_words = sort_ctas(g, max_tiles) * kRadixBins;
     PRK_TRY(tmp.alloc((void **)&counts, (size_t)count_words * sizeof(int32_t)));
     PRK_TRY(tmp.alloc((void **)&offsets, (size_t)(count_words + 1) * sizeof(int32_t)));
     int64_t desc_words = (n + 1 + kScanTile - 1) / kScanTile;
@@ -1085,7 +1137,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     // (keys are class * 64 + bucket)
     int32_t h_cls[4];
     for (int q = 0; q < 4; ++q)
-        PRK_CUDA(cudaMemcpyAsync(&h_cls[q], offsets + (int64_t)(q + 1) * 64 * order_tiles, sizeof(int32_t),
+        PRK_CUDA(cudaMemcpyAsync(&h_cls[q], offsets + (int64_t)(q + 1) * 64 * sort_ctas(g, order_tiles), sizeof(int32_t),
                                  cudaMemcpyDeviceToHost, s), "class counts");
     PRK_TRY(check_timeout());
     g->n_c = h_cls[0];
