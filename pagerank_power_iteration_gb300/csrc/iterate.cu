@@ -58,6 +58,7 @@ struct IterArgs {
     const int32_t *deg_out;   // out-degrees by vertex id
     const int32_t *w_split;   // [warps + 1]: warp-class rows of each warp of the grid
     int64_t n, n_c, n_w, n_t, n_z, n_chunks;
+    int64_t t_short;          // first thread-class block whose rows span at most two int4s
 };
 
 // streaming (evict-first) loads of the index stream
@@ -203,27 +204,86 @@ __device__ __forceinline__ RowBlock load_row_block(const int32_t *__restrict__ w
     return b;
 }
 
-// Row sum of a thread-class row, lane j owning row j of a block of cnt <= 32
-// consecutive rows. The rows of a block all span len int4s, stored
-// interleaved: int4 k of row j at blk + k * cnt + j, so a warp's loads are
-// coalesced. Up to four int4s (16 gathers) per lane in flight.
+// Thread-class rows: lane j owns row j of a block of cnt <= 32 consecutive
+// work rows. The rows of a block all span len int4s, stored interleaved
+// (int4 k of row j at blk + k * cnt + j), so a warp's loads are coalesced.
 template <typename T>
-__device__ __forceinline__ T lane_row_sum(const int4 *__restrict__ blk, int32_t len, int32_t cnt,
-                                          const Gather<T> &gat)
+struct LaneRow {
+    int32_t off;       // this lane's first int4 (index into the work CSR)
+    int32_t len, cnt;  // int4s per row (0: no row in this lane), rows in the block
+    int32_t deg;       // out-degree and old state, for the combine
+    T so;
+};
+
+// Lane rows of the block at work row r0 (rows past t_end are inactive).
+template <typename T>
+__device__ __forceinline__ LaneRow<T> load_lane_row(const IterArgs<T> &a, const T *__restrict__ s_old, int64_t r0,
+                                                    int64_t t_end, int lane)
+{
+    LaneRow<T> r;
+    const int64_t i = r0 + lane;
+    const bool act = i < t_end;
+    r.cnt = (int)min((int64_t)32, t_end - r0);
+    const int32_t nb = i <= t_end ? a.w_ptr[i] : 0;
+    int32_t ne = __shfl_down_sync(0xffffffffu, nb, 1);
+    if (lane == 31 && r0 + 32 <= t_end)
+        ne = a.w_ptr[r0 + 32];
+    r.off = (__shfl_sync(0xffffffffu, nb, 0) >> 2) + lane;
+    r.len = act ? (ne - nb) >> 2 : 0;   // every thread-class row spans at least one int4
+    r.deg = 0;
+    r.so = T(0);
+    if (act) {
+        r.deg = a.w_deg[i];
+        r.so = s_old[i];
+    }
+    return r;
+}
+
+// Row sum of one lane row, up to four int4s (16 gathers) in flight.
+template <typename T>
+__device__ __forceinline__ T lane_row_sum(const LaneRow<T> &R, const int4 *__restrict__ cv, const Gather<T> &gat)
 {
     T y = T(0);
-    for (int32_t k = 0; k < len; k += 4) {
+    for (int32_t k = 0; k < R.len; k += 4) {
         int4 q[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-            if (k + t < len)
-                q[t] = ld_stream4(blk + (k + t) * cnt);
+            if (k + t < R.len)
+                q[t] = ld_stream4(cv + R.off + (k + t) * R.cnt);
 #pragma unroll
         for (int t = 0; t < 4; ++t)
-            if (k + t < len)
+            if (k + t < R.len)
                 y += gat.four(q[t]);
     }
     return y;
+}
+
+// Row sums of two lane rows of at most two int4s each (A and B, from two
+// blocks), all their loads in flight at once. Each row adds its int4s in order.
+template <typename T>
+__device__ __forceinline__ void short_row_sums2(const LaneRow<T> &A, const LaneRow<T> &B,
+                                                const int4 *__restrict__ cv, const Gather<T> &gat, T &ya, T &yb)
+{
+    int4 qa0, qa1, qb0, qb1;
+    const bool a0 = 0 < A.len, a1 = 1 < A.len, b0 = 0 < B.len, b1 = 1 < B.len;
+    if (a0)
+        qa0 = ld_stream4(cv + A.off);
+    if (a1)
+        qa1 = ld_stream4(cv + A.off + A.cnt);
+    if (b0)
+        qb0 = ld_stream4(cv + B.off);
+    if (b1)
+        qb1 = ld_stream4(cv + B.off + B.cnt);
+    ya = T(0);
+    yb = T(0);
+    if (a0)
+        ya += gat.four(qa0);
+    if (a1)
+        ya += gat.four(qa1);
+    if (b0)
+        yb += gat.four(qb0);
+    if (b1)
+        yb += gat.four(qb1);
 }
 
 // Row sums of a block of up to 32 consecutive work rows, each padded to
@@ -397,9 +457,11 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     // range of rows, cut so that every warp has about the same edges
     // (w_split), and streams each block's int4s (block_row_sums).
     // Thread-class rows: the warps of the grid sweep the blocks round-robin,
-    // one row per lane, the block stored interleaved (lane_row_sum). The old state and out-degree of a
-    // block's rows are loaded before its gathers, and the next block's
-    // offsets while they are in flight.
+    // one row per lane, the blocks stored interleaved: blocks of long rows
+    // one at a time (lane_row_sum), blocks of short rows two at a time
+    // (short_row_sums2). The old state and out-degree of a block's
+    // rows are loaded before its gathers; in the warp class, the next block's
+    // offsets are loaded while they are in flight.
     {
         const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
         const int64_t r_begin = a.w_split[gw], r_end = a.w_split[gw + 1];
@@ -424,36 +486,28 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         }
 
         const int64_t t_begin = a.n_c + a.n_w, t_end = t_begin + a.n_t;
-        const int64_t t_stride = G * kWarps * 32;
-        int64_t r0 = t_begin + gw * 32;
-        if (r0 < t_end) {
-            int32_t nb = r0 + lane <= t_end ? a.w_ptr[r0 + lane] : 0;
-            int32_t ne = __shfl_down_sync(0xffffffffu, nb, 1);
-            if (lane == 31 && r0 + 32 <= t_end)
-                ne = a.w_ptr[r0 + 32];
-            for (; r0 < t_end; r0 += t_stride) {
-                const int64_t i = r0 + lane;
-                const bool act = i < t_end;
-                const int cnt = (int)min((int64_t)32, t_end - r0);
-                const int32_t blk4 = __shfl_sync(0xffffffffu, nb, 0) >> 2;   // the block's first int4
-                const int32_t len = act ? (ne - nb) >> 2 : 0;
-                int32_t deg = 0;
-                T so = T(0);
-                if (act) {
-                    deg = a.w_deg[i];
-                    so = s_old[i];
-                }
-                const int64_t r1 = r0 + t_stride;
-                if (r1 < t_end) {
-                    nb = r1 + lane <= t_end ? a.w_ptr[r1 + lane] : 0;
-                    ne = __shfl_down_sync(0xffffffffu, nb, 1);
-                    if (lane == 31 && r1 + 32 <= t_end)
-                        ne = a.w_ptr[r1 + 32];
-                }
-                const T y = lane_row_sum(cv + blk4 + lane, len, cnt, gat);
-                if (act)
-                    combine_row(i, y, deg, so, s_new, base, d, l1, dm);
-            }
+        const int64_t nw = G * kWarps;
+        const int64_t t_blocks = (t_end - t_begin + 31) / 32;
+        const int64_t t_short = min(a.t_short, t_blocks);
+        // rows of three to eight int4s: one block per warp at a time
+        for (int64_t bb = gw; bb < t_short; bb += nw) {
+            const LaneRow<T> A = load_lane_row(a, s_old, t_begin + bb * 32, t_end, lane);
+            const T y = lane_row_sum(A, cv, gat);
+            if (A.len > 0)
+                combine_row(t_begin + bb * 32 + lane, y, A.deg, A.so, s_new, base, d, l1, dm);
+        }
+        // rows of one or two int4s: two blocks per warp at a time
+        for (int64_t bb = t_short + gw; bb < t_blocks; bb += 2 * nw) {
+            const bool has_b = bb + nw < t_blocks;   // warp-uniform
+            const LaneRow<T> A = load_lane_row(a, s_old, t_begin + bb * 32, t_end, lane);
+            const LaneRow<T> B = has_b ? load_lane_row(a, s_old, t_begin + (bb + nw) * 32, t_end, lane)
+                                       : LaneRow<T>{0, 0, 1, 0, T(0)};
+            T ya, yb;
+            short_row_sums2(A, B, cv, gat, ya, yb);
+            if (A.len > 0)
+                combine_row(t_begin + bb * 32 + lane, ya, A.deg, A.so, s_new, base, d, l1, dm);
+            if (B.len > 0)
+                combine_row(t_begin + (bb + nw) * 32 + lane, yb, B.deg, B.so, s_new, base, d, l1, dm);
         }
     }
 
@@ -625,6 +679,7 @@ IterArgs<T> make_args(pr_graph *g)
     a.n_t = g->n_t;
     a.n_z = g->n_z;
     a.n_chunks = g->n_chunks;
+    a.t_short = g->t_short;
     return a;
 }
 

@@ -99,6 +99,9 @@ struct pr_graph {
     int32_t *chunk_first = nullptr;  // [n_c + 1]: first chunk of each CTA row
     uint32_t *hub_arrivals = nullptr; // [n_c]: chunks of the row finished this update
     int64_t n_dangling = 0, n_z = 0, n_t = 0, n_w = 0, n_c = 0, n_chunks = 0;
+    // thread-class rows come in blocks of 32 sorted by length, longest first;
+    // blocks [t_short, ...) have rows of at most two int4s
+    int64_t t_short = 0;
     int64_t e_t = 0, e_w = 0, e_c = 0;
 
     prk::Scalars *scal = nullptr;   // device

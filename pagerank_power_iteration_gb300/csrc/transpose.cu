@@ -367,20 +367,22 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     __shared__ int32_t s_val[kPadTile];
     __shared__ int64_t s_row_lo, s_row_hi;
 
+    // positions are below count <= 2^31 - 1: 32-bit indexing throughout
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t c = blockIdx.x;
-    const int64_t t_first = tile_lo(c, tiles, ctas), t_last = tile_lo(c + 1, tiles, ctas);
+    const int32_t t_first = (int32_t)tile_lo(c, tiles, ctas), t_last = (int32_t)tile_lo(c + 1, tiles, ctas);
+    const int32_t n_keys = (int32_t)count;
     s_run[tid] = (unsigned)offsets[(int64_t)tid * ctas + c];
 
     int32_t key[kRadixItems], val[kRadixItems];
     unsigned rank[kRadixItems];
     // keys (and values) of tile t into registers
-    auto load_tile = [&](int64_t t) {
-        const int64_t base = t * kRadixTile + (int64_t)warp * kWarpSpan;
+    auto load_tile = [&](int32_t t) {
+        const int32_t base = t * kRadixTile + warp * kWarpSpan;
 #pragma unroll
         for (int r = 0; r < kRadixItems; ++r) {
-            const int64_t i = base + r * 32 + lane;
-            const bool ok = i < count;
+            const int32_t i = base + r * 32 + lane;
+            const bool ok = i < n_keys;
             key[r] = ok ? keys_in[i] : 0;
             if (!(kFlags & kSrcRows))
                 val[r] = ok ? vals_in[i] : 0;
@@ -389,13 +391,13 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     if (t_first < t_last)
         load_tile(t_first);
 
-    for (int64_t tile = t_first; tile < t_last; ++tile) {
+    for (int32_t tile = t_first; tile < t_last; ++tile) {
         __syncthreads();   // the previous tile's shared-memory reads are done
         for (int w = 0; w < kWarps; ++w)
             s_wh[w][tid] = 0;
-        const int64_t tile_begin = tile * kRadixTile;
-        const int tile_count = (int)min((int64_t)kRadixTile, count - tile_begin);
-        const int64_t base = tile_begin + (int64_t)warp * kWarpSpan;
+        const int32_t tile_begin = tile * kRadixTile;
+        const int tile_count = min(kRadixTile, n_keys - tile_begin);
+        const int32_t base = tile_begin + warp * kWarpSpan;
 
         if (kFlags & kSrcRows) {
             // row of every position of the tile: mark row starts, then max-scan.
@@ -430,7 +432,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         const unsigned below = (1u << lane) - 1u;
 #pragma unroll
         for (int r = 0; r < kRadixItems; ++r) {
-            const bool ok = base + r * 32 + lane < count;
+            const bool ok = base + r * 32 + lane < n_keys;
             const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
             const unsigned peers = __match_any_sync(0xffffffffu, dig);
             const unsigned before = ok ? s_wh[warp][dig] : 0u;
@@ -469,7 +471,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         // stage the tile in (digit, input) order
 #pragma unroll
         for (int r = 0; r < kRadixItems; ++r) {
-            if (base + r * 32 + lane < count) {
+            if (base + r * 32 + lane < n_keys) {
                 const unsigned dig = ((unsigned)key[r] >> shift) & (kRadixBins - 1);
                 const int lp = (int)(s_start[dig] + s_wh[warp][dig] + rank[r]);
                 s_key[spad(lp)] = key[r];
@@ -490,7 +492,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
                 const int32_t kv = s_key[spad(i)];
                 const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
                 const unsigned pos = s_delta[dig] + (unsigned)i;
-                if ((int64_t)pos >= count)   // only reachable if the offsets scan failed
+                if (pos >= (unsigned)n_keys)   // only reachable if the offsets scan failed
                     continue;
                 vals_out[pos] = s_val[spad(i)];
                 if (kFlags & kWriteKeys)
@@ -765,6 +767,25 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
     }
 }
 
+// First thread-class block (32 work rows from t_begin) whose rows span at
+// most two int4s; t_blocks if there is none. Block lengths never increase
+// (the work order sorts these rows by length, longest first), so one thread
+// bisects.
+__global__ void k_first_short_block(const int32_t *__restrict__ w_ptr, int64_t t_begin, int64_t t_blocks,
+                                    unsigned long long *out)
+{
+    int64_t lo = 0, hi = t_blocks;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) / 2;
+        const int64_t r = t_begin + 32 * mid;
+        if (w_ptr[r + 1] - w_ptr[r] <= 8)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    *out = (unsigned long long)lo;
+}
+
 __global__ void k_permute_deg(int64_t n, const int32_t *__restrict__ order,
                               const int32_t *__restrict__ deg_out, int32_t *__restrict__ w_deg)
 {
@@ -1026,7 +1047,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
 
     // scratch
     int32_t *in_deg = nullptr;
-    unsigned long long *counters = nullptr;   // [0] = dangling, [1..3] = class edges
+    unsigned long long *counters = nullptr;   // [0] dangling, [1..3] class edges, [4] t_short
     unsigned *tile_counter = nullptr;
     unsigned long long *desc = nullptr;
     int32_t *counts = nullptr, *offsets = nullptr;   // digit-major tile counts and their scan
@@ -1191,7 +1212,12 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
             c_end, g->n_c, g->n_c + g->n_w, g->in_ptr, g->order, counters + 1);
         ++g->build_launches;
     }
-    unsigned long long h_counters[4] = {0, 0, 0, 0};
+    if (g->n_t > 0) {
+        k_first_short_block<<<1, 1, 0, s>>>(g->w_ptr, g->n_c + g->n_w, (g->n_t + 31) / 32, counters + 4);
+        ++g->build_launches;
+    }
+    PRK_CUDA(cudaGetLastError(), "short-block launch");
+    unsigned long long h_counters[5] = {0, 0, 0, 0, 0};
     PRK_CUDA(cudaMemcpyAsync(h_counters, counters, sizeof(h_counters), cudaMemcpyDeviceToHost, s),
              "counters");
     PRK_TRY(check_timeout());
@@ -1199,6 +1225,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     g->e_c = (int64_t)h_counters[1];
     g->e_w = (int64_t)h_counters[2];
     g->e_t = (int64_t)h_counters[3];
+    g->t_short = (int64_t)h_counters[4];
     return PR_OK;
 #undef PRK_TRY
 #undef PRK_CUDA
