@@ -373,9 +373,26 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
 
     // the head of the state vector, where the work order puts the most
     // gathered vertices, staged in shared memory for this update
+    // (16-byte copies, all of a thread's loads in flight before its stores;
+    // both buffers are 16-byte aligned)
     T *s_hot = reinterpret_cast<T *>(s_dyn);
-    for (int32_t u = tid; u < hot; u += kIterBlock)
-        s_hot[u] = s_old[u];
+    {
+        constexpr int kPer = (kHotBytes / 16 + kIterBlock - 1) / kIterBlock;
+        const int32_t hot4 = (int32_t)((int64_t)hot * (int64_t)sizeof(T) / 16);
+        const int4 *src = reinterpret_cast<const int4 *>(s_old);
+        int4 *dst = reinterpret_cast<int4 *>(s_hot);
+        int4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+            if (tid + k * kIterBlock < hot4)
+                v[k] = __ldcg(src + tid + k * kIterBlock);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+            if (tid + k * kIterBlock < hot4)
+                dst[tid + k * kIterBlock] = v[k];
+        for (int32_t u = (int32_t)(hot4 * 16 / (int32_t)sizeof(T)) + tid; u < hot; u += kIterBlock)
+            s_hot[u] = s_old[u];
+    }
     __syncthreads();
     const Gather<T> gat{s_old, s_hot, hot};
 
@@ -511,14 +528,22 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         }
     }
 
-    // rows without in-edges: x' = base; four rows per thread in flight
+    // rows without in-edges: x' = base; eight rows per thread in flight
     {
         const int64_t z0 = a.n - a.n_z, stride = G * kIterBlock;
-        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < a.n; i += 4 * stride) {
+        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < a.n; i += 8 * stride) {
+            int32_t dg[8];
+            T so[8];
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
+            for (int t = 0; t < 8; ++t)
+                if (i + t * stride < a.n) {
+                    dg[t] = a.w_deg[i + t * stride];
+                    so[t] = s_old[i + t * stride];
+                }
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
                 if (i + t * stride < a.n)
-                    finish_row(i + t * stride, T(0), a.w_deg, s_old, s_new, base, d, l1, dm);
+                    combine_row(i + t * stride, T(0), dg[t], so[t], s_new, base, d, l1, dm);
         }
     }
 
