@@ -27,7 +27,38 @@ def gpu():
     oracle.build()
 
 
+def graph_with_in_degrees(degs, n, seed):
+    """A graph on n vertices whose first len(degs) vertices (in a shuffled order)
+    have the given in-degrees, from distinct random sources; the other vertices
+    have no in-edges. Out-degrees follow from the draw (some sources dangle)."""
+    rng = np.random.default_rng(seed)
+    rows = rng.permutation(n)[: len(degs)]
+    src, dst = [], []
+    for v, k in zip(rows, degs):
+        src.append(rng.choice(n, size=k, replace=False))
+        dst.append(np.full(k, v))
+    return gg.from_edges(n, np.concatenate(src), np.concatenate(dst))
+
+
+def layout_degrees():
+    """In-degrees that cover the work layout's edges: every thread-class length
+    1..32 (so 32-row blocks mix padded lengths and the split between long and
+    short blocks falls inside a block), warp-class rows at the 4-edge padding
+    and 128-edge step boundaries up to 1024, hub rows around the 512-edge
+    chunks, and a row count that is not a multiple of 32."""
+    degs = list(range(1, 33)) * 37
+    degs += [33, 34, 35, 36, 64, 127, 128, 129, 255, 256, 511, 512, 513, 1000, 1023, 1024] * 3
+    degs += [1025, 1536, 2048, 2049, 5000]
+    return degs
+
+
 def graph(name):
+    if name == "layout":
+        return graph_with_in_degrees(layout_degrees(), 9011, seed=7)
+    if name == "t_short_only":   # thread-class rows of one or two int4s only
+        return graph_with_in_degrees([1 + i % 8 for i in range(999)], 4001, seed=8)
+    if name == "t_long_only":    # thread-class rows of three to eight int4s only
+        return graph_with_in_degrees([9 + i % 24 for i in range(1001)], 4003, seed=9)
     if name in ("tiny", "single", "nodangling", "dangling", "star", "chain"):
         return day40_case(name)
     if name == "star_out":
@@ -59,7 +90,7 @@ def graph(name):
 
 SMALL = ["tiny", "single", "nodangling", "dangling", "star", "chain", "star_out", "no_edges",
          "all_dangling_but_one", "selfloops1", "dups_loops", "hub70k", "n257", "n65537",
-         "citation30k", "rmat14", "er16"]
+         "citation30k", "rmat14", "er16", "layout", "t_short_only", "t_long_only"]
 
 
 @pytest.mark.parametrize("name", SMALL + ["rmat18"])
@@ -107,14 +138,14 @@ def test_converged_ranks_f32(name):
     _parity(rp, ci, "f32")
 
 
-@pytest.mark.parametrize("name", ["tiny", "dangling", "star", "chain", "dups_loops", "hub70k",
-                                  "citation30k", "rmat14", "er16"])
+@pytest.mark.parametrize("name", ["tiny", "dangling", "star", "chain", "dups_loops", "hub70k", "layout",
+                                  "citation30k", "rmat14", "er16", "layout", "t_short_only", "t_long_only"])
 def test_converged_ranks_f64(name):
     rp, ci = graph(name)
     _parity(rp, ci, "f64", tol=1e-10, max_iter=400)
 
 
-@pytest.mark.parametrize("name", ["dangling", "citation30k", "rmat14"])
+@pytest.mark.parametrize("name", ["dangling", "citation30k", "rmat14", "layout"])
 @pytest.mark.parametrize("dtype", ["f32", "f64"])
 def test_fixed_iterations(name, dtype):
     """tol <= 0 runs exactly max_iter updates (the timed fixed-50 mode)."""
@@ -185,7 +216,7 @@ def test_host_and_device_buffers_agree():
     assert np.array_equal(xa.cpu().numpy(), xc.cpu().numpy())
 
 
-@pytest.mark.parametrize("name", ["rmat18", "citation30k", "hub70k"])
+@pytest.mark.parametrize("name", ["rmat18", "citation30k", "hub70k", "layout"])
 def test_runs_repeat_bit_for_bit(name):
     """Every sum is formed in a fixed order and L1 / D are exact fixed-point
     sums, so repeated runs (and a second handle) give identical bits."""
