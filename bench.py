@@ -65,6 +65,8 @@ def parse_args(argv=None):
                    help="updates in the oracle's CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-library", action="store_true",
+                   help="skip the library-composed comparator (torch sort + cuSPARSE SpMV)")
     return p.parse_args(argv)
 
 
@@ -337,7 +339,11 @@ def run_ours(args, rank, world, local_rank, dist):
 
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, rp, ci, n, m, dev, tdt, d, dist)
+    if rank == 0 and not args.no_library:
+        line["library_comparator"] = run_library(rp, ci, d, args.tol, args.max_iter, tdt, dev,
+                                                 ours=out, ours_updates=iters[-1])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_multicore"] = time_cpu_parallel(rp, ci, d, args.cpu_updates)
         dt, _ = time_oracle(rp, ci, d, args.cpu_updates)
         line["cpu_baseline"] = {
             "value": round(m * args.cpu_updates / dt / 1e9, 5), "unit": UNIT, "cores": 1,
@@ -347,6 +353,78 @@ def run_ours(args, rank, world, local_rank, dist):
             **host_info(),
         }
     return line
+
+
+def time_cpu_parallel(rp, ci, d, updates):
+    """The multi-core CPU baseline (OpenMP pull, fp64, all host cores) on the full
+    workload: its parallel transpose plus a fixed number of updates."""
+    import cpu_parallel
+    cpu_parallel.build()
+    m = len(ci)
+    r = cpu_parallel.pagerank(rp, ci, d, tol=0.0, max_iter=updates)
+    return {"value": round(m * r["iters"] / r["t_loop"] / 1e9, 4), "unit": UNIT, "cores": r["threads"],
+            "kind": "openmp pull over the in-edge CSR, fp64", "transpose_s": round(r["t_transpose"], 3),
+            "loop_s": round(r["t_loop"], 3),
+            "step_gteps": round(m * r["iters"] / (r["t_transpose"] + r["t_loop"]) / 1e9, 4),
+            "sample": f"full graph: the parallel transpose + {r['iters']} fixed fp64 updates"}
+
+
+def library_pagerank(rp, ci, d, tol, max_iter, tdt, dev, fixed=None):
+    """The same method composed from library calls, timed beside ours: the
+    transpose as a library sort of (destination, source) keys, each update as
+    a cuSPARSE CSR SpMV (torch.mv on a sparse CSR tensor) over x/outdeg plus
+    torch elementwise ops and reductions for the dangling mass, the combine
+    and the L1 distance. The loop checks L1 on the host after every update,
+    as the library composition of Day 40 does; `fixed` runs exactly that many
+    updates with no check. Returns (x, updates, transpose_ms, loop_ms)."""
+    import torch
+    n, m = len(rp) - 1, len(ci)
+    outdeg = torch.from_numpy(np.diff(rp)).to(dev)
+    start, mid, end = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize(dev)
+    start.record()
+    dst = torch.from_numpy(ci).to(dev).long()
+    src = torch.repeat_interleave(torch.arange(n, device=dev), outdeg)
+    key, _ = torch.sort(dst * n + src)
+    crow = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+    crow[1:] = torch.cumsum(torch.bincount(dst, minlength=n), 0)
+    a = torch.sparse_csr_tensor(crow, key % n, torch.ones(m, dtype=tdt, device=dev), size=(n, n))
+    del key, src, dst
+    mid.record()
+    dang = (outdeg == 0).to(tdt)
+    inv = torch.where(outdeg > 0, 1.0 / outdeg.clamp(min=1).to(tdt), torch.zeros((), dtype=tdt, device=dev))
+    x = torch.full((n,), 1.0 / n, dtype=tdt, device=dev)
+    updates = 0
+    while updates < (fixed or max_iter):
+        y = torch.mv(a, x * inv)
+        dm = torch.dot(x, dang)
+        xn = (1.0 - d) / n + d * (y + dm / n)
+        l1 = torch.sum(torch.abs(xn - x))
+        x = xn
+        updates += 1
+        if fixed is None and tol > 0 and float(l1) < tol:
+            break
+    end.record()
+    torch.cuda.synchronize(dev)
+    return x, updates, start.elapsed_time(mid), mid.elapsed_time(end)
+
+
+def run_library(rp, ci, d, tol, max_iter, tdt, dev, ours=None, ours_updates=None):
+    """Library-composed comparator: a warm-up call, then one timed call."""
+    import torch
+    m = len(ci)
+    library_pagerank(rp, ci, d, tol, max_iter, tdt, dev, fixed=2)
+    x, ups, t_ms, loop_ms = library_pagerank(rp, ci, d, tol, max_iter, tdt, dev)
+    res = {"impl": "torch.sort transpose + cuSPARSE CSR SpMV (torch.mv) + torch elementwise and "
+                   "reductions; L1 read on the host after every update",
+           "updates": ups, "transpose_ms": round(t_ms, 3), "time_to_converge_ms": round(loop_ms, 3),
+           "ms_per_update": round(loop_ms / max(ups, 1), 5),
+           "iteration_gteps": round(m * ups / (loop_ms * 1e-3) / 1e9, 3),
+           "step_gteps": round(m * ups / ((t_ms + loop_ms) * 1e-3) / 1e9, 3)}
+    if ours is not None and ours_updates == ups:
+        xo = ours.to(x.dtype)
+        res["max_rel_diff_vs_ours"] = float(torch.max(torch.abs(x - xo) / torch.clamp(torch.abs(xo), min=1e-30)))
+    return res
 
 
 def run_e2e(args, rp, ci, n, m, dev, tdt, d, dist):
