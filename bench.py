@@ -410,11 +410,13 @@ def library_pagerank(rp, ci, d, tol, max_iter, tdt, dev, fixed=None):
 
 
 def run_library(rp, ci, d, tol, max_iter, tdt, dev, ours=None, ours_updates=None):
-    """Library-composed comparator: a warm-up call, then one timed call."""
+    """Library-composed comparator: a warm-up call, then the best of two timed calls."""
     import torch
     m = len(ci)
     library_pagerank(rp, ci, d, tol, max_iter, tdt, dev, fixed=2)
-    x, ups, t_ms, loop_ms = library_pagerank(rp, ci, d, tol, max_iter, tdt, dev)
+    runs = [library_pagerank(rp, ci, d, tol, max_iter, tdt, dev) for _ in range(2)]
+    x, ups = runs[-1][0], runs[-1][1]
+    t_ms, loop_ms = min(r[2] for r in runs), min(r[3] for r in runs)
     res = {"impl": "torch.sort transpose + cuSPARSE CSR SpMV (torch.mv) + torch elementwise and "
                    "reductions; L1 read on the host after every update",
            "updates": ups, "transpose_ms": round(t_ms, 3), "time_to_converge_ms": round(loop_ms, 3),
