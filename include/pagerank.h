@@ -81,8 +81,8 @@ typedef struct pr_graph_info {
     int64_t n, m;
     int64_t n_dangling;         /* vertices with out-degree 0 */
     int64_t rows_zero;          /* in-degree 0: no gather */
-    int64_t rows_thread;        /* in-degree 1..32: one thread per row */
-    int64_t rows_warp;          /* in-degree 33..1024: one warp per row */
+    int64_t rows_thread;        /* in-degree 1..32: one lane per row */
+    int64_t rows_warp;          /* in-degree 33..1024: 32-row blocks, one warp each */
     int64_t rows_cta;           /* in-degree > 1024: split into chunks streamed by CTAs */
     int64_t edges_thread, edges_warp, edges_cta;
     int64_t cta_chunks;         /* number of CTA chunks */

@@ -13,11 +13,14 @@
 //   - the pull SpMV gathers s over the class-major work CSR (the in-edge CSR
 //     relabelled so that each in-degree class is one contiguous range of rows
 //     and edges, see transpose.cu), by class: rows above 1024 in-edges are
-//     streamed by whole CTAs, 512 edges per warp, whose partial sums the warp
-//     finishing the row's last chunk adds up in chunk order (no CTA-wide
-//     barrier); one warp per row for 33..1024;
-//     one thread per row for 1..32; rows without in-edges take the constant
-//     term only. CTA and warp rows are padded to whole 16-byte index loads;
+//     streamed in 512-edge chunks, each warp a contiguous range of chunks,
+//     and the warp that completes a row adds its pieces in chunk order (no
+//     CTA-wide barrier); rows of 33..1024 in-edges are taken 32 consecutive
+//     rows at a time by one warp that streams their int4s flat and forms the
+//     row sums with a segmented scan; rows of 1..32 in-edges one per lane,
+//     sorted by length and stored interleaved by blocks of 32; rows without
+//     in-edges take the constant term only. Every row is padded to whole
+//     16-byte index loads;
 //   - the combine reads D from device memory (Day 40, "Keep the dangling mass
 //     on the device"), writes s' and accumulates the L1 distance and the next
 //     dangling mass;

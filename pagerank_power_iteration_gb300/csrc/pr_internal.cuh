@@ -16,8 +16,8 @@ namespace prk {
 // In-degree classes of the pull SpMV (gpu-graph-study, "PageRank T4 -
 // degree-bucketed load balancing": thread per row up to 32, warp per row up
 // to 1024, block per row above). Rows above kWarpMax are cut into chunks of
-// kChunkEdges edges, one warp each, so that a CTA streams 8 consecutive
-// chunks and one hub is spread over many CTAs.
+// kChunkEdges edges; each warp of the update kernel streams one contiguous
+// range of chunks, so one hub is spread over many warps and CTAs.
 constexpr int kThreadMax = 32;
 constexpr int kWarpMax = 1024;
 constexpr int kChunkEdges = 512;

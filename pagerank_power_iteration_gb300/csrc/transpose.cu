@@ -28,7 +28,8 @@
 // and 0) give the class-major work order: one more stable counting-sort pass
 // over the vertices, keyed by class (CTA rows first, then warp, thread and
 // zero rows) and, inside a class, by half-octave bucket of the out-degree,
-// largest first (ties by id).
+// largest first; thread-class rows by padded length first, longest first,
+// then by a coarse out-degree bucket (ties by id; see k_order_keys).
 //
 // Work layout. The iteration does not run on the in-edge CSR above (which is
 // kept, bit for bit, for pr_get_in_csr) but on the same graph relabelled by
