@@ -101,9 +101,21 @@ def measured_peak_hbm():
         return 6800.0, "fallback"
 
 
+def code_digest(text: str) -> str:
+    """sha256 (first 16 hex digits) of C/CUDA source with its comments, blank
+    lines and trailing spaces removed, so that editing a comment does not
+    orphan a profile taken on the same code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()[:16]
+
+
 def kernel_source_digest() -> str:
-    with open(os.path.join(ROOT, "pagerank_power_iteration_gb300", "csrc", "iterate.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Code digest of the update kernel's source file (and of the header it includes)."""
+    csrc = os.path.join(ROOT, "pagerank_power_iteration_gb300", "csrc")
+    text = "".join(open(os.path.join(csrc, f)).read() for f in ("iterate.cu", "pr_internal.cuh"))
+    return code_digest(text)
 
 
 def profiled_traffic(workload: str):

@@ -99,3 +99,12 @@ def test_aggregate_over_two_gloo_ranks():
 
 def test_aggregate_without_process_group():
     assert bench.aggregate(None, "cpu", 12.5, 77.0) == (12.5, 77.0)
+
+
+def test_code_digest_ignores_comments_but_not_code():
+    import bench
+    a = "int f(int x) {\n    return x + 1;   // add one\n}\n"
+    b = "/* header */\nint f(int x) {\n\n    return x + 1;\n}\n"
+    c = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench.code_digest(a) == bench.code_digest(b)
+    assert bench.code_digest(a) != bench.code_digest(c)
