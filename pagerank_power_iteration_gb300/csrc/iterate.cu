@@ -13,7 +13,7 @@
 //   - the pull SpMV gathers s over the class-major work CSR (the in-edge CSR
 //     relabelled so that each in-degree class is one contiguous range of rows
 //     and edges, see transpose.cu), by class: rows above 1024 in-edges are
-//     streamed in 512-edge chunks, each warp a contiguous range of chunks,
+//     streamed in 256-edge chunks, each warp a contiguous range of chunks,
 //     and the warp that completes a row adds its pieces in chunk order (no
 //     CTA-wide barrier); rows of 33..1024 in-edges are taken 32 consecutive
 //     rows at a time by one warp that streams their int4s flat and forms the

@@ -20,7 +20,7 @@ namespace prk {
 // range of chunks, so one hub is spread over many warps and CTAs.
 constexpr int kThreadMax = 32;
 constexpr int kWarpMax = 1024;
-constexpr int kChunkEdges = 512;
+constexpr int kChunkEdges = 256;
 constexpr int kBlock = 256;        // CTA size of the preprocessing kernels
 constexpr int kIterBlock = 1024;   // CTA size of the update kernel (one CTA per SM)
 constexpr int kHotBytes = 160 * 1024;   // shared-memory copy of the state's head

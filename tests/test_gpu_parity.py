@@ -44,7 +44,7 @@ def layout_degrees():
     """In-degrees that cover the work layout's edges: every thread-class length
     1..32 (so 32-row blocks mix padded lengths and the split between long and
     short blocks falls inside a block), warp-class rows at the 4-edge padding
-    and 128-edge step boundaries up to 1024, hub rows around the 512-edge
+    and 128-edge step boundaries up to 1024, hub rows around the 256-edge
     chunks, and a row count that is not a multiple of 32."""
     degs = list(range(1, 33)) * 37
     degs += [33, 34, 35, 36, 64, 127, 128, 129, 255, 256, 511, 512, 513, 1000, 1023, 1024] * 3
