@@ -458,11 +458,14 @@ def run_e2e(args, rp, ci, n, m, dev, tdt, d, dist):
     if dist is not None:
         dist.barrier()
     edges = 0
+    step_ms = []
     t0 = time.perf_counter()
     for _ in range(k):
+        ts = time.perf_counter()
         g = prg.Graph(rp_h, ci_h)
-        _, it, _, _ = g.run(d, args.tol, args.max_iter, dtype=tdt, out=out_h)
+        _, it, _, _ = g.run(d, args.tol, args.max_iter, dtype=tdt, out=out_h)   # synchronises
         g.close()
+        step_ms.append((time.perf_counter() - ts) * 1e3)
         edges += m * it
     torch.cuda.synchronize(dev)
     ms, edges = aggregate(dist, dev, (time.perf_counter() - t0) * 1e3, float(edges))
@@ -471,6 +474,7 @@ def run_e2e(args, rp, ci, n, m, dev, tdt, d, dist):
     return {"value": round(edges / dt / 1e9, 3), "unit": UNIT,
             "h2d_bytes_per_step": 8 * (n + 1) + 4 * m, "d2h_bytes_per_step": elt * n,
             "steps": k, "ms_per_step": round(dt / k * 1e3, 3),
+            "step_ms_min_max": [round(min(step_ms), 3), round(max(step_ms), 3)],
             "api": "Graph(pinned host CSR) + Graph.run(out=pinned host tensor)"}
 
 
