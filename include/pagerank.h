@@ -108,7 +108,10 @@ typedef struct pr_run_stats {
 /*
  * Builds the device-side graph from an out-edge CSR.
  *   n        number of vertices (1 <= n <= 2^31 - 2)
- *   m        number of edges (0 <= m <= 2^31 - 1)
+ *   m        number of edges (0 <= m <= 2^31 - 1), and in addition
+ *            m + 3 min(n, m) + PR_LAYOUT_SLACK <= 2^31 - 1: the work layout
+ *            pads every row with in-edges to a multiple of 4 entries and keeps
+ *            int32 offsets; larger graphs get PR_ERR_TOO_LARGE
  *   row_ptr  int64[n + 1], row_ptr[0] = 0, non-decreasing, row_ptr[n] = m;
  *            the out-edges of u are col_idx[row_ptr[u] .. row_ptr[u+1])
  *   col_idx  int32[m], targets in [0, n); duplicates and self-loops are kept
@@ -158,6 +161,9 @@ pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info);
 
 /* Fills *stats with the statistics of the handle's most recent pr_run. */
 pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
+
+/* Padding slack of the work layout in pr_graph_create's size limit. */
+#define PR_LAYOUT_SLACK 8192
 
 /* Largest `count` that pr_exclusive_scan_noalloc accepts (2^26). */
 #define PR_SCAN_NOALLOC_MAX (1LL << 26)

@@ -23,7 +23,7 @@ __all__ = [
     "PageRankError", "pr_graph_info", "pr_run_stats", "lib", "library_path",
     "pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info", "pr_graph_last_run",
     "pr_graph_destroy", "pr_last_error", "pr_version", "pr_exclusive_scan_noalloc",
-    "PR_SCAN_NOALLOC_MAX", "Graph", "EXPORTED_SYMBOLS",
+    "PR_SCAN_NOALLOC_MAX", "PR_LAYOUT_SLACK", "max_edges", "Graph", "EXPORTED_SYMBOLS",
 ]
 
 PR_OK = 0
@@ -41,6 +41,18 @@ EXPORTED_SYMBOLS = ("pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_
                     "pr_graph_last_run", "pr_graph_destroy", "pr_last_error", "pr_version",
                     "pr_exclusive_scan_noalloc")
 PR_SCAN_NOALLOC_MAX = 1 << 26
+PR_LAYOUT_SLACK = 8192
+
+
+def max_edges(n: int) -> int:
+    """Largest m that pr_graph_create accepts for n vertices: m <= 2^31 - 1 and
+    m + 3 min(n, m) + PR_LAYOUT_SLACK <= 2^31 - 1 (the padded work layout keeps
+    int32 offsets)."""
+    cap = (1 << 31) - 1
+    best = cap - PR_LAYOUT_SLACK - 3 * n          # when n <= m
+    if best >= n:
+        return min(cap, best)
+    return (cap - PR_LAYOUT_SLACK) // 4           # when m < n: m + 3m <= cap - slack
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libpagerank_gb300.so")

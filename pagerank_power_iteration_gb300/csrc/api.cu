@@ -120,6 +120,11 @@ namespace {
 
 constexpr int64_t kMaxN = ((int64_t)1 << 31) - 2;
 constexpr int64_t kMaxM = ((int64_t)1 << 31) - 1;
+// The work CSR pads every row that has in-edges to a multiple of 4 entries
+// (at most 3 more per row, and at most min(n, m) such rows), and the few
+// thread-class blocks that mix row lengths pad their rows to the block's
+// longest (under 8192 entries in all); its offsets are int32.
+constexpr int64_t kLayoutSlack = PR_LAYOUT_SLACK;
 
 // Restores the caller's current device on scope exit.
 struct DeviceGuard {
@@ -174,6 +179,11 @@ PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
         return set_error(PR_ERR_TOO_LARGE, "n = %lld exceeds 2^31 - 2", (long long)n);
     if (m > kMaxM)
         return set_error(PR_ERR_TOO_LARGE, "m = %lld exceeds 2^31 - 1", (long long)m);
+    if (m + 3 * (n < m ? n : m) + kLayoutSlack > kMaxM)
+        return set_error(PR_ERR_TOO_LARGE,
+                         "m + 3 min(n, m) + %lld = %lld exceeds 2^31 - 1 (the padded work layout keeps "
+                         "int32 offsets)", (long long)kLayoutSlack,
+                         (long long)(m + 3 * (n < m ? n : m) + kLayoutSlack));
     if (row_ptr == nullptr)
         return set_error(PR_ERR_INVALID_ARG, "row_ptr is NULL");
     if (m > 0 && col_idx == nullptr)

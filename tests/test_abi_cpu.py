@@ -92,3 +92,28 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(prg, "library_path", str(tmp_path / "nope.so"))
     with pytest.raises(prg.PageRankError):
         prg.lib()
+
+
+def test_create_rejects_graphs_whose_padded_layout_overflows(L):
+    # m + 3 min(n, m) + PR_LAYOUT_SLACK must fit in int32 (checked on the host,
+    # before any device work or dereference of the inputs)
+    rp = (ctypes.c_int64 * 2)(0, 0)
+    ci = (ctypes.c_int32 * 1)(0)
+    h = ctypes.c_void_p()
+    for n in (1 << 24, 1000, (1 << 31) - 2):
+        m = prg.max_edges(n) + 1
+        st = L.pr_graph_create(n, m, ctypes.addressof(rp), ctypes.addressof(ci), None, ctypes.byref(h))
+        assert st == prg.PR_ERR_TOO_LARGE and not h.value, (n, m)
+        assert "int32" in prg.pr_last_error()
+    # the limit itself: every extra edge past max_edges(n) breaks the bound
+    for n in (1 << 24, 1000, (1 << 31) - 2):
+        m = prg.max_edges(n)
+        assert m + 3 * min(n, m) + prg.PR_LAYOUT_SLACK <= (1 << 31) - 1
+        m1 = m + 1
+        assert m1 + 3 * min(n, m1) + prg.PR_LAYOUT_SLACK > (1 << 31) - 1 or m1 > (1 << 31) - 1
+
+
+def test_layout_slack_matches_the_header():
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(prg.__file__)), "include", "pagerank.h")).read()
+    assert int(re.search(r"#define PR_LAYOUT_SLACK (\d+)", hdr).group(1)) == prg.PR_LAYOUT_SLACK
