@@ -39,6 +39,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "PageRank GTEPS/iteration and time-to-converge; % of HBM roofline"
 UNIT = "GTEPS"
+GATHER_PROBE = 1 << 27   # gathers per pass of the gather-rate measurement
 GRAPH_DESC = {
     "rmat24": "RMAT scale 24, edge factor 16, a/b/c/d=.57/.19/.19/.05, seed 4, dedup, no self-loops",
     "rmat22": "RMAT scale 22, edge factor 16, a/b/c/d=.57/.19/.19/.05, seed 3, dedup, no self-loops",
@@ -347,6 +348,21 @@ def run_ours(args, rank, world, local_rank, dist):
         },
         "clocks": clocks,
         "host_wall_s": round(wall, 3), "generate_s": round(gen_s, 2),
+    }
+
+    # the bound that holds the update: gathers not served from shared memory,
+    # against the random-gather rate of this GPU measured here
+    hot = int(info["edges_hot_f32" if args.dtype == "f32" else "edges_hot_f64"])
+    l2_gathers = m - hot
+    g_peak = prg.pr_measure_gather_rate(n, dcode, GATHER_PROBE, sp)
+    g_ach = l2_gathers / (per_update_ms * 1e-3)
+    line["gather_roofline"] = {
+        "bound": "l2 random gather", "achieved": round(g_ach / 1e9, 2),
+        "peak": round(g_peak / 1e9, 2), "unit": "G gathers/s",
+        "frac": round(g_ach / g_peak, 4),
+        "l2_gathers_per_update": l2_gathers, "smem_gathers_per_update": hot,
+        "peak_source": f"pr_measure_gather_rate: {GATHER_PROBE} uniform random gathers from an "
+                       f"{n}-element {args.dtype} state (the run's working set), measured in this run",
     }
 
     if not args.no_e2e:

@@ -91,6 +91,12 @@ typedef struct pr_graph_info {
     int32_t iterate_grid;       /* CTAs of the persistent iteration kernel */
     int64_t device_bytes;       /* device memory held by the handle */
     int32_t build_launches;     /* kernels pr_graph_create launched */
+    int64_t edges_hot_f32;      /* in-edges whose source is in the head of the state
+                                   vector that every update copies into each SM's
+                                   shared memory (fp32 runs: 40,960 vertices); their
+                                   gathers never reach L2, the other m - edges_hot
+                                   gathers do */
+    int64_t edges_hot_f64;      /* the same for fp64 runs (20,480 vertices) */
 } pr_graph_info;
 
 /* Statistics of the most recent pr_run on a handle (filled by pr_graph_last_run). */
@@ -196,6 +202,30 @@ pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
  */
 pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
                                     void *stream);
+
+/*
+ * Measures the current GPU's rate of random gathers: loads of single dtype
+ * elements from uniformly random positions of an n-element state vector,
+ * each of which misses L1 and costs one L2 request. This is the bound of the
+ * update's gathers that the shared-memory copy of the state's head does not
+ * serve (those are m - edges_hot per update, see pr_graph_info), so a run's
+ * rate of such gathers can be reported as a fraction of it. The pages have
+ * no counterpart: it is the denominator of the update kernel's gather
+ * roofline. The indices are drawn on the device (SplitMix64 of the position,
+ * reduced mod n) and streamed as int32; the time is that of three passes
+ * after a warm-up, taken with CUDA events on `stream`.
+ *   n             elements of the state vector, 1 <= n <= 2^31 - 2 (pass the
+ *                 graph's n to measure at the run's working-set size)
+ *   dtype         PR_F32 or PR_F64: the element type gathered
+ *   gathers       gathers per pass, 1 <= gathers <= 2^30 (about 2^27 gives a
+ *                 pass of a few tenths of a millisecond)
+ *   gathers_per_s receives the measured rate
+ * Allocates n * sizeof(dtype) + 4 * gathers bytes from the library's pool
+ * for the duration of the call and synchronizes `stream`. Returns PR_OK,
+ * PR_ERR_INVALID_ARG, PR_ERR_OOM or PR_ERR_CUDA.
+ */
+pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathers,
+                                 double *gathers_per_s, void *stream);
 
 /* Frees the handle and returns all device memory it owns to the library's
  * pool (see the handle's description). NULL is ignored. The

@@ -23,7 +23,7 @@ __all__ = [
     "PageRankError", "pr_graph_info", "pr_run_stats", "lib", "library_path",
     "pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info", "pr_graph_last_run",
     "pr_graph_destroy", "pr_last_error", "pr_version", "pr_exclusive_scan_noalloc",
-    "PR_SCAN_NOALLOC_MAX", "PR_LAYOUT_SLACK", "max_edges", "Graph", "EXPORTED_SYMBOLS",
+    "pr_measure_gather_rate", "PR_SCAN_NOALLOC_MAX", "PR_LAYOUT_SLACK", "max_edges", "Graph", "EXPORTED_SYMBOLS",
 ]
 
 PR_OK = 0
@@ -39,7 +39,7 @@ PR_F64 = 1
 
 EXPORTED_SYMBOLS = ("pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info",
                     "pr_graph_last_run", "pr_graph_destroy", "pr_last_error", "pr_version",
-                    "pr_exclusive_scan_noalloc")
+                    "pr_exclusive_scan_noalloc", "pr_measure_gather_rate")
 PR_SCAN_NOALLOC_MAX = 1 << 26
 PR_LAYOUT_SLACK = 8192
 
@@ -73,7 +73,8 @@ class pr_graph_info(ctypes.Structure):
                 ("edges_thread", ctypes.c_int64), ("edges_warp", ctypes.c_int64),
                 ("edges_cta", ctypes.c_int64), ("cta_chunks", ctypes.c_int64),
                 ("cta_chunk_edges", ctypes.c_int32), ("iterate_grid", ctypes.c_int32),
-                ("device_bytes", ctypes.c_int64), ("build_launches", ctypes.c_int32)]
+                ("device_bytes", ctypes.c_int64), ("build_launches", ctypes.c_int32),
+                ("edges_hot_f32", ctypes.c_int64), ("edges_hot_f64", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
@@ -123,6 +124,8 @@ def lib():
         L.pr_version.restype = ctypes.c_char_p
         L.pr_exclusive_scan_noalloc.argtypes = [vp, vp, i64, vp]
         L.pr_exclusive_scan_noalloc.restype = ctypes.c_int
+        L.pr_measure_gather_rate.argtypes = [i64, ctypes.c_int, i64, ctypes.POINTER(dbl), vp]
+        L.pr_measure_gather_rate.restype = ctypes.c_int
         _lib = L
         return L
 
@@ -175,6 +178,15 @@ def pr_exclusive_scan_noalloc(counts: int, offsets: int, count: int, stream: int
     Allocates no device memory (static scratch for up to PR_SCAN_NOALLOC_MAX
     elements, shared by all calls: do not overlap calls on the GPU)."""
     _check(lib().pr_exclusive_scan_noalloc(counts, offsets, count, stream))
+
+
+def pr_measure_gather_rate(n: int, dtype: int, gathers: int, stream: int | None = None) -> float:
+    """Raw call. Random gathers per second from an n-element state vector of
+    dtype (PR_F32 or PR_F64) on the current GPU: the ceiling of the update's
+    gathers that shared memory does not serve."""
+    rate = ctypes.c_double(0.0)
+    _check(lib().pr_measure_gather_rate(n, dtype, gathers, ctypes.byref(rate), stream))
+    return rate.value
 
 
 def pr_last_error() -> str:

@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libpagerank_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["api.cu", "transpose.cu", "iterate.cu"]
+SOURCES = ["api.cu", "transpose.cu", "iterate.cu", "calibrate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]

@@ -335,7 +335,24 @@ PR_API pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info)
     info->iterate_grid = g->st[0].ready ? g->st[0].grid : g->st[1].grid;
     info->device_bytes = g->device_bytes;
     info->build_launches = g->build_launches;
+    info->edges_hot_f32 = g->e_hot[0];
+    info->edges_hot_f64 = g->e_hot[1];
     return PR_OK;
+}
+
+PR_API pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathers,
+                                        double *gathers_per_s, void *stream)
+{
+    if (gathers_per_s == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "gathers_per_s is NULL");
+    if (n < 1 || n > kMaxN)
+        return set_error(PR_ERR_INVALID_ARG, "n must be in [1, 2^31 - 2] (got %lld)", (long long)n);
+    if (gathers < 1 || gathers > ((int64_t)1 << 30))
+        return set_error(PR_ERR_INVALID_ARG, "gathers must be in [1, 2^30] (got %lld)",
+                         (long long)gathers);
+    if (dtype != PR_F32 && dtype != PR_F64)
+        return set_error(PR_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    return prk::measure_gather_rate(n, (int)dtype, gathers, gathers_per_s, (cudaStream_t)stream);
 }
 
 PR_API pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats)

@@ -24,6 +24,8 @@ constexpr int kChunkEdges = 256;
 constexpr int kBlock = 256;        // CTA size of the preprocessing kernels
 constexpr int kIterBlock = 1024;   // CTA size of the update kernel (one CTA per SM)
 constexpr int kHotBytes = 160 * 1024;   // shared-memory copy of the state's head
+constexpr int32_t kHotF32 = kHotBytes / 4;   // state entries in that copy, fp32 runs
+constexpr int32_t kHotF64 = kHotBytes / 8;   // and fp64 runs
 // Per-row cost, in edges, added to the edges when warp-class rows are split
 // over the warps of the update kernel. The flat 32-row blocks make the
 // per-row work small: a pure edge balance (0) measured best (RMAT-24 update
@@ -105,6 +107,7 @@ struct pr_graph {
     // blocks [t_short, ...) have rows of at most two int4s
     int64_t t_short = 0;
     int64_t e_t = 0, e_w = 0, e_c = 0;
+    int64_t e_hot[2] = {0, 0};     // in-edges with a source in the hot head, fp32 / fp64
 
     prk::Scalars *scal = nullptr;   // device
     unsigned *err = nullptr;        // device error word
@@ -150,6 +153,9 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
 pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
                                  cudaStream_t s);
 constexpr int kMaxDevices = 64;
+
+// Random-gather rate of the current GPU (calibrate.cu).
+pr_status measure_gather_rate(int64_t n, int dtype, int64_t gathers, double *rate, cudaStream_t s);
 
 // Iteration (iterate.cu).
 pr_status run(pr_graph *g, double d, double tol, int32_t max_iter, int dtype,

@@ -727,17 +727,30 @@ __global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *
 // [w_ptr[r0] / 4, w_ptr[r0] / 4 + cnt * L), and int4 k of the block's row j
 // sits at w_ptr[r0] / 4 + k * cnt + j, so that the lanes of a warp, one row
 // each, read consecutive int4s.
+//
+// The kernel also counts the edges whose relabelled source falls in the head
+// of the state vector that the update keeps in shared memory, for fp32
+// (kHotF32 vertices) and fp64 (kHotF64) runs: hot[0] and hot[1] (zeroed by
+// the caller).
 __global__ void __launch_bounds__(kBlock)
 k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t rows_end,
           const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_first,
           const int32_t *__restrict__ w_ptr, const int32_t *__restrict__ order,
           const int32_t *__restrict__ perm, const int32_t *__restrict__ in_ptr,
-          const int32_t *__restrict__ in_col, int32_t *__restrict__ w_col)
+          const int32_t *__restrict__ in_col, int32_t *__restrict__ w_col,
+          unsigned long long *__restrict__ hot)
 {
     const int lane = threadIdx.x & 31;
     const int64_t gtid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gwarp = gtid >> 5, nwarps = nthreads >> 5;
+    unsigned long long h32 = 0, h64 = 0;
+    auto relabel = [&](int32_t u) {
+        const int32_t w = perm[u];
+        h32 += (w < kHotF32);
+        h64 += (w < kHotF64);
+        return w;
+    };
     for (int64_t c = gwarp; c < n_chunks; c += nwarps) {
         const int32_t r = chunk_row[c];
         const int32_t v = order[r];
@@ -746,14 +759,14 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
         const int32_t k0 = (int32_t)(c - chunk_first[r]) * kChunkEdges;
         const int32_t k1 = min(k0 + kChunkEdges, len);
         for (int32_t k = k0 + lane; k < k1; k += 32)
-            w_col[dst + k] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
+            w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
     }
     for (int64_t i = n_c + gwarp; i < wide_end; i += nwarps) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
         for (int32_t k = lane; k < len; k += 32)
-            w_col[dst + k] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
+            w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
     }
     for (int64_t i = wide_end + gtid; i < rows_end; i += nthreads) {
         const int32_t v = order[i];
@@ -764,7 +777,16 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
         const int64_t blk = w_ptr[r0];
         const int32_t len = w_ptr[i + 1] - w_ptr[i];
         for (int32_t k = 0; k < len; ++k)
-            w_col[blk + 4 * ((k >> 2) * cnt + j) + (k & 3)] = (k < deg) ? perm[in_col[src + k]] : kPadSource;
+            w_col[blk + 4 * ((k >> 2) * cnt + j) + (k & 3)] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        h32 += __shfl_xor_sync(0xffffffffu, h32, o);
+        h64 += __shfl_xor_sync(0xffffffffu, h64, o);
+    }
+    if (lane == 0 && h32) {
+        atomicAdd(hot, h32);
+        atomicAdd(hot + 1, h64);
     }
 }
 
@@ -1048,7 +1070,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
 
     // scratch
     int32_t *in_deg = nullptr;
-    unsigned long long *counters = nullptr;   // [0] dangling, [1..3] class edges, [4] t_short
+    unsigned long long *counters = nullptr;   // [0] dangling, [1..3] class edges, [4] t_short,
+                                              // [5..6] edges with a hot source (fp32, fp64)
     unsigned *tile_counter = nullptr;
     unsigned long long *desc = nullptr;
     int32_t *counts = nullptr, *offsets = nullptr;   // digit-major tile counts and their scan
@@ -1201,7 +1224,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         k_relabel<<<g->num_sms * 8, kBlock, 0, s>>>(n, g->n_c, g->n_chunks, g->n_c + g->n_w,
                                                      g->n_c + g->n_w + g->n_t, g->chunk_row,
                                                      g->chunk_first, g->w_ptr, g->order, g->perm,
-                                                     g->in_ptr, g->in_col, g->w_col);
+                                                     g->in_ptr, g->in_col, g->w_col, counters + 5);
         ++g->build_launches;
     }
     PRK_CUDA(cudaGetLastError(), "relabel launch");
@@ -1218,7 +1241,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         ++g->build_launches;
     }
     PRK_CUDA(cudaGetLastError(), "short-block launch");
-    unsigned long long h_counters[5] = {0, 0, 0, 0, 0};
+    unsigned long long h_counters[7] = {0, 0, 0, 0, 0, 0, 0};
     PRK_CUDA(cudaMemcpyAsync(h_counters, counters, sizeof(h_counters), cudaMemcpyDeviceToHost, s),
              "counters");
     PRK_TRY(check_timeout());
@@ -1227,6 +1250,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     g->e_w = (int64_t)h_counters[2];
     g->e_t = (int64_t)h_counters[3];
     g->t_short = (int64_t)h_counters[4];
+    g->e_hot[0] = (int64_t)h_counters[5];
+    g->e_hot[1] = (int64_t)h_counters[6];
     return PR_OK;
 #undef PRK_TRY
 #undef PRK_CUDA

@@ -87,6 +87,16 @@ def test_run_rejects_bad_arguments_on_host(L, d, tol, max_iter, dtype):
     assert st == prg.PR_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("n,dtype,gathers", [(0, 0, 1024), (-5, 0, 1024), ((1 << 31) - 1, 0, 1024),
+                                              (1000, 0, 0), (1000, 0, (1 << 30) + 1), (1000, 7, 1024)])
+def test_gather_rate_rejects_bad_arguments_on_host(L, n, dtype, gathers):
+    rate = ctypes.c_double(0.0)
+    assert L.pr_measure_gather_rate(1000, 0, 1024, None, None) == prg.PR_ERR_INVALID_ARG
+    st = L.pr_measure_gather_rate(n, dtype, gathers, ctypes.byref(rate), None)
+    assert st == prg.PR_ERR_INVALID_ARG
+    assert rate.value == 0.0
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(prg, "_lib", None)
     monkeypatch.setattr(prg, "library_path", str(tmp_path / "nope.so"))

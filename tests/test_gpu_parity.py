@@ -111,6 +111,39 @@ def test_transpose_bit_exact(name):
     assert info["n_dangling"] == int((np.diff(rp) == 0).sum())
 
 
+def work_order(rp, ci):
+    """The documented class-major work order, derived independently on the host:
+    rows with in-degree > 1024, then 33..1024, then 1..32, then 0; inside the
+    first two classes by half-octave bucket of the out-degree, largest first;
+    thread-class rows by padded length in int4s (longest first), then by a coarse
+    out-degree bucket; ties by vertex id."""
+    n = len(rp) - 1
+    indeg = np.bincount(ci, minlength=n).astype(np.int64)
+    outdeg = np.diff(rp).astype(np.int64)
+    cls = np.select([indeg > 1024, indeg > 32, indeg > 0], [0, 1, 2], 3)
+    x = outdeg + 1
+    b = np.floor(np.log2(x)).astype(np.int64)
+    half = np.where(b > 0, (x >> np.maximum(b - 1, 0)) & 1, 0)
+    ob = np.minimum(63, 2 * b + half)
+    sub = np.where(cls == 2, (8 - ((indeg + 3) >> 2)) * 8 + (7 - np.minimum(7, ob >> 2)), 63 - ob)
+    return np.argsort(cls * 64 + sub, kind="stable")
+
+
+@pytest.mark.parametrize("name", ["layout", "rmat18", "citation30k"])
+def test_hot_source_edge_counts(name):
+    """edges_hot_* counts the in-edges whose source is among the first 40,960
+    (fp32) or 20,480 (fp64) vertices of the work order: every out-edge of such a
+    vertex, so the count is the sum of their out-degrees."""
+    rp, ci = graph(name)
+    with prg.Graph(rp, ci) as g:
+        info = g.info()
+    outdeg = np.diff(rp)
+    order = work_order(rp, ci)
+    assert info["edges_hot_f32"] == int(outdeg[order[:40960]].sum())
+    assert info["edges_hot_f64"] == int(outdeg[order[:20480]].sum())
+    assert 0 <= info["edges_hot_f64"] <= info["edges_hot_f32"] <= info["m"]
+
+
 def _parity(rp, ci, dtype, tol=1e-6, max_iter=200, check_iters=True):
     tt = {"f32": torch.float32, "f64": torch.float64}[dtype]
     tolset = F32 if dtype == "f32" else F64
