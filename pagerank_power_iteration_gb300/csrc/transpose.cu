@@ -222,7 +222,12 @@ __global__ void k_outdeg(int64_t n, const int64_t *__restrict__ row_ptr,
 
 constexpr int kRadixBits = 8;
 constexpr int kRadixBins = 1 << kRadixBits;
-constexpr int kRadixItems = 8;
+// Keys per thread of a counting-sort tile (256 threads). Measured on the
+// transpose of RMAT-24 / ER-24 / RMAT-22 with four CTAs per SM: 8 keys 9.25 /
+// 10.95 / 2.68 ms per pr_graph_create, 12 keys 8.86 / 10.11 / 2.60 ms; 16 keys
+// need fewer CTAs per SM (registers) and lost (three per SM 9.20 / 10.13 /
+// 2.67, two per SM 10.54 / 10.71 / 3.00).
+constexpr int kRadixItems = 12;
 constexpr int kRadixTile = kBlock * kRadixItems;
 
 // Tiles [tile_lo(c), tile_lo(c + 1)) of a pass belong to CTA c of `ctas`:
@@ -310,15 +315,21 @@ enum : unsigned { kSrcRows = 1u, kWriteKeys = 2u, kHistogram = 4u };
 __device__ __forceinline__ int spad(int i) { return i + (i >> 5); }   // bank-conflict padding
 
 // Block-wide inclusive max-scan of the kRadixTile entries of `a` (16-byte
-// aligned, unpadded), kRadixItems = 8 consecutive entries per thread, read
-// and written as two int4s.
+// aligned, unpadded), kRadixItems consecutive entries per thread, read and
+// written as whole int4s.
 __device__ __forceinline__ void block_max_scan(int32_t *a, int32_t *s_wmax)
 {
-    static_assert(kRadixItems == 8, "two int4s per thread");
+    static_assert(kRadixItems % 4 == 0, "whole int4s per thread");
+    constexpr int kQ = kRadixItems / 4;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int4 *a4 = reinterpret_cast<int4 *>(a) + 2 * tid;
-    int4 q0 = a4[0], q1 = a4[1];
-    const int32_t run = max(max(max(q0.x, q0.y), max(q0.z, q0.w)), max(max(q1.x, q1.y), max(q1.z, q1.w)));
+    int4 *a4 = reinterpret_cast<int4 *>(a) + kQ * tid;
+    int4 q[kQ];
+    int32_t run = INT32_MIN;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+        q[k] = a4[k];
+        run = max(run, max(max(q[k].x, q[k].y), max(q[k].z, q[k].w)));
+    }
     int32_t incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -335,16 +346,14 @@ __device__ __forceinline__ void block_max_scan(int32_t *a, int32_t *s_wmax)
     const int32_t up = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane > 0)
         carry = max(carry, up);
-    q0.x = carry = max(carry, q0.x);
-    q0.y = carry = max(carry, q0.y);
-    q0.z = carry = max(carry, q0.z);
-    q0.w = carry = max(carry, q0.w);
-    q1.x = carry = max(carry, q1.x);
-    q1.y = carry = max(carry, q1.y);
-    q1.z = carry = max(carry, q1.z);
-    q1.w = carry = max(carry, q1.w);
-    a4[0] = q0;
-    a4[1] = q1;
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) {
+        q[k].x = carry = max(carry, q[k].x);
+        q[k].y = carry = max(carry, q[k].y);
+        q[k].z = carry = max(carry, q[k].z);
+        q[k].w = carry = max(carry, q[k].w);
+        a4[k] = q[k];
+    }
     __syncthreads();
 }
 
@@ -410,8 +419,9 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
                 s_row_hi = vals_in[tile + 1];
             }
             const int4 none = make_int4(INT32_MIN, INT32_MIN, INT32_MIN, INT32_MIN);
-            reinterpret_cast<int4 *>(rmap)[2 * tid] = none;
-            reinterpret_cast<int4 *>(rmap)[2 * tid + 1] = none;
+#pragma unroll
+            for (int k = 0; k < kRadixItems / 4; ++k)
+                reinterpret_cast<int4 *>(rmap)[(kRadixItems / 4) * tid + k] = none;
             __syncthreads();
             const int64_t rlo = s_row_lo, rhi = s_row_hi;
             if (tid == 0)
