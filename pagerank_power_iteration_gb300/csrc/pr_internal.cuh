@@ -111,7 +111,7 @@ struct pr_graph {
 
     prk::Scalars *scal = nullptr;   // device
     unsigned *err = nullptr;        // device error word
-    prk::Scalars *h_scal = nullptr; // pinned host mirror
+    prk::Scalars *h_scal = nullptr; // host mirror (pageable), read after each run
 
     prk::DtypeState st[2];
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
