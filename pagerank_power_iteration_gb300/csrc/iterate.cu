@@ -218,21 +218,43 @@ struct LaneRow {
     T so;
 };
 
-// Lane rows of the block at work row r0 (rows past t_end are inactive).
+// Where a thread-class block lies in the work CSR: its first int4 and the
+// length in int4s that all its rows share (the block's first row is its
+// longest, and every row of the block is padded to that length).
+struct BlockDesc {
+    int32_t off4, len4;
+};
+
+// Lane j reads the descriptor of block b0 + j * stride (j < 32, blocks below
+// nblocks; the others get an empty one). A warp reads the descriptors of its
+// next 32 blocks at once, so the index loads of a block never wait on w_ptr.
+__device__ __forceinline__ BlockDesc load_block_descs(const int32_t *__restrict__ w_ptr, int64_t t_begin,
+                                                      int64_t b0, int64_t stride, int64_t nblocks, int lane)
+{
+    BlockDesc d{0, 0};
+    const int64_t b = b0 + (int64_t)lane * stride;
+    if (b < nblocks) {
+        const int64_t r = t_begin + b * 32;
+        const int32_t p = w_ptr[r];
+        d.off4 = p >> 2;
+        d.len4 = (w_ptr[r + 1] - p) >> 2;   // every thread-class row spans at least one int4
+    }
+    return d;
+}
+
+// Lane rows of the block at work row r0 (rows past t_end are inactive), the
+// block's placement taken from lane k's descriptor.
 template <typename T>
-__device__ __forceinline__ LaneRow<T> load_lane_row(const IterArgs<T> &a, const T *__restrict__ s_old, int64_t r0,
-                                                    int64_t t_end, int lane)
+__device__ __forceinline__ LaneRow<T> lane_row_of(const IterArgs<T> &a, const T *__restrict__ s_old, int64_t r0,
+                                                  int64_t t_end, const BlockDesc &desc, int k, int lane)
 {
     LaneRow<T> r;
     const int64_t i = r0 + lane;
     const bool act = i < t_end;
     r.cnt = (int)min((int64_t)32, t_end - r0);
-    const int32_t nb = i <= t_end ? a.w_ptr[i] : 0;
-    int32_t ne = __shfl_down_sync(0xffffffffu, nb, 1);
-    if (lane == 31 && r0 + 32 <= t_end)
-        ne = a.w_ptr[r0 + 32];
-    r.off = (__shfl_sync(0xffffffffu, nb, 0) >> 2) + lane;
-    r.len = act ? (ne - nb) >> 2 : 0;   // every thread-class row spans at least one int4
+    r.off = __shfl_sync(0xffffffffu, desc.off4, k) + lane;
+    const int32_t len = __shfl_sync(0xffffffffu, desc.len4, k);
+    r.len = act ? len : 0;
     r.deg = 0;
     r.so = T(0);
     if (act) {
@@ -509,25 +531,40 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         const int64_t nw = G * kWarps;
         const int64_t t_blocks = (t_end - t_begin + 31) / 32;
         const int64_t t_short = min(a.t_short, t_blocks);
-        // rows of three to eight int4s: one block per warp at a time
-        for (int64_t bb = gw; bb < t_short; bb += nw) {
-            const LaneRow<T> A = load_lane_row(a, s_old, t_begin + bb * 32, t_end, lane);
-            const T y = lane_row_sum(A, cv, gat);
-            if (A.len > 0)
-                combine_row(t_begin + bb * 32 + lane, y, A.deg, A.so, s_new, base, d, l1, dm);
+        // rows of three to eight int4s: one block per warp at a time (blocks
+        // gw, gw + nw, ...), their descriptors read 32 blocks ahead
+        for (int64_t b0 = gw; b0 < t_short; b0 += 32 * nw) {
+            const BlockDesc desc = load_block_descs(a.w_ptr, t_begin, b0, nw, t_short, lane);
+            for (int k = 0; k < 32; ++k) {
+                const int64_t bb = b0 + k * nw;
+                if (bb >= t_short)   // warp-uniform
+                    break;
+                const LaneRow<T> A = lane_row_of(a, s_old, t_begin + bb * 32, t_end, desc, k, lane);
+                const T y = lane_row_sum(A, cv, gat);
+                if (A.len > 0)
+                    combine_row(t_begin + bb * 32 + lane, y, A.deg, A.so, s_new, base, d, l1, dm);
+            }
         }
-        // rows of one or two int4s: two blocks per warp at a time
-        for (int64_t bb = t_short + gw; bb < t_blocks; bb += 2 * nw) {
-            const bool has_b = bb + nw < t_blocks;   // warp-uniform
-            const LaneRow<T> A = load_lane_row(a, s_old, t_begin + bb * 32, t_end, lane);
-            const LaneRow<T> B = has_b ? load_lane_row(a, s_old, t_begin + (bb + nw) * 32, t_end, lane)
-                                       : LaneRow<T>{0, 0, 1, 0, T(0)};
-            T ya, yb;
-            short_row_sums2(A, B, cv, gat, ya, yb);
-            if (A.len > 0)
-                combine_row(t_begin + bb * 32 + lane, ya, A.deg, A.so, s_new, base, d, l1, dm);
-            if (B.len > 0)
-                combine_row(t_begin + (bb + nw) * 32 + lane, yb, B.deg, B.so, s_new, base, d, l1, dm);
+        // rows of one or two int4s: two blocks per warp at a time (blocks bb
+        // and bb + nw, bb = t_short + gw, then every 2 nw), descriptors read
+        // 16 pairs ahead
+        for (int64_t b0 = t_short + gw; b0 < t_blocks; b0 += 32 * nw) {
+            const BlockDesc desc = load_block_descs(a.w_ptr, t_begin, b0, nw, t_blocks, lane);
+            for (int k = 0; k < 32; k += 2) {
+                const int64_t bb = b0 + k * nw;
+                if (bb >= t_blocks)   // warp-uniform
+                    break;
+                const bool has_b = bb + nw < t_blocks;   // warp-uniform
+                const LaneRow<T> A = lane_row_of(a, s_old, t_begin + bb * 32, t_end, desc, k, lane);
+                const LaneRow<T> B = has_b ? lane_row_of(a, s_old, t_begin + (bb + nw) * 32, t_end, desc, k + 1, lane)
+                                           : LaneRow<T>{0, 0, 1, 0, T(0)};
+                T ya, yb;
+                short_row_sums2(A, B, cv, gat, ya, yb);
+                if (A.len > 0)
+                    combine_row(t_begin + bb * 32 + lane, ya, A.deg, A.so, s_new, base, d, l1, dm);
+                if (B.len > 0)
+                    combine_row(t_begin + (bb + nw) * 32 + lane, yb, B.deg, B.so, s_new, base, d, l1, dm);
+            }
         }
     }
 
