@@ -434,7 +434,8 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     // that completes the count adds the pieces in chunk order and combines
     // the row. No CTA-wide barrier, and no wait.
     const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
-    {
+    const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
+    auto phase_hub = [&]() {
         const int64_t nwarps = G * kWarps;
         const int64_t per = (a.n_chunks + nwarps - 1) / nwarps;
         const int64_t c_end = min((gw + 1) * per, a.n_chunks);
@@ -492,7 +493,7 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
             }
             c = stop;
         }
-    }
+    };
 
     // warp class (33..1024 in-edges) and thread class (1..32), in blocks of
     // 32 consecutive rows. Warp-class rows: each warp owns one contiguous
@@ -504,8 +505,7 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     // (short_row_sums2). The old state and out-degree of a block's
     // rows are loaded before its gathers; in the warp class, the next block's
     // offsets are loaded while they are in flight.
-    {
-        const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
+    auto phase_warp = [&]() {
         const int64_t r_begin = a.w_split[gw], r_end = a.w_split[gw + 1];
         if (r_begin < r_end) {
             RowBlock nb = load_row_block(a.w_ptr, r_begin, (int)min((int64_t)32, r_end - r_begin), lane);
@@ -526,7 +526,8 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
                     combine_row(r0 + lane, y, deg, so, s_new, base, d, l1, dm);
             }
         }
-
+    };
+    auto phase_thread = [&]() {
         const int64_t t_begin = a.n_c + a.n_w, t_end = t_begin + a.n_t;
         const int64_t nw = G * kWarps;
         const int64_t t_blocks = (t_end - t_begin + 31) / 32;
@@ -566,6 +567,27 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
                     combine_row(t_begin + (bb + nw) * 32 + lane, yb, B.deg, B.so, s_new, base, d, l1, dm);
             }
         }
+    };
+    // Each warp takes the three gather phases in its own order: warp w of the
+    // CTA starts with phase w % 3 (hub, warp-class, thread-class) and wraps
+    // around. Every SM then runs all three at once, and the thread class,
+    // whose short rows leave few gathers in flight per warp, overlaps the
+    // streaming classes instead of running alone at the end of the update.
+    // What a warp computes does not depend on the order (no phase waits on
+    // another, and the L1 and D totals are exact), so results are unchanged.
+    const int rot = warp % 3;
+    if (rot == 0) {
+        phase_hub();
+        phase_warp();
+        phase_thread();
+    } else if (rot == 1) {
+        phase_warp();
+        phase_thread();
+        phase_hub();
+    } else {
+        phase_thread();
+        phase_hub();
+        phase_warp();
     }
 
     // rows without in-edges: x' = base; eight rows per thread in flight
