@@ -61,7 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--dtype", choices=["f32", "f64"], default="f32")
     p.add_argument("--tol", type=float, default=1e-6)
     p.add_argument("--max-iter", type=int, default=200)
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-updates", type=int, default=2,
                    help="updates in the oracle's CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
