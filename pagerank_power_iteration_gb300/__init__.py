@@ -216,6 +216,27 @@ def _ptr(a) -> int | None:
     return a.data_ptr()
 
 
+def _check_vector(a, n: int, dtype, name: str) -> None:
+    """Raises unless ``a`` (numpy array or torch tensor) holds exactly n
+    contiguous values of ``dtype`` (torch.float32 or torch.float64)."""
+    import torch
+    if isinstance(a, np.ndarray):
+        want = np.float32 if dtype == torch.float32 else np.float64
+        if a.dtype != want:
+            raise TypeError(f"{name} must be {np.dtype(want).name}, got {a.dtype}")
+        size, contiguous = a.size, a.flags["C_CONTIGUOUS"]
+    elif isinstance(a, torch.Tensor):
+        if a.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {a.dtype}")
+        size, contiguous = a.numel(), a.is_contiguous()
+    else:
+        raise TypeError(f"{name} must be a numpy array or a torch tensor")
+    if size != n:
+        raise ValueError(f"{name} must hold n = {n} values, got {size}")
+    if not contiguous:
+        raise ValueError(f"{name} must be contiguous")
+
+
 def _stream(stream):
     import torch
     if stream is None:
@@ -262,12 +283,17 @@ class Graph:
         """
         import torch
         dtype = torch.float32 if dtype is None else dtype
-        code = {torch.float32: PR_F32, torch.float64: PR_F64}[dtype]
+        if dtype not in (torch.float32, torch.float64):
+            raise TypeError("dtype must be torch.float32 or torch.float64")
+        code = PR_F32 if dtype == torch.float32 else PR_F64
         if out is None:
             out = torch.empty(self.n, dtype=dtype, device=f"cuda:{self.device}")
-        if x_init is not None and not isinstance(x_init, np.ndarray):
-            if x_init.dtype != dtype:
-                raise TypeError("x_init must have the run's dtype")
+        # the library reads and writes exactly n values of the run's type
+        # through these pointers, so a shorter buffer or another type would be
+        # read or written out of bounds
+        _check_vector(out, self.n, dtype, "out")
+        if x_init is not None:
+            _check_vector(x_init, self.n, dtype, "x_init")
         st, it, l1 = pr_run(self._h, float(d), float(tol), int(max_iter), code, _ptr(out),
                             _ptr(x_init), _stream(stream))
         return out, it, l1, st == PR_OK

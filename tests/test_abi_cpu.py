@@ -127,3 +127,32 @@ def test_layout_slack_matches_the_header():
     import re
     hdr = open(os.path.join(os.path.dirname(os.path.dirname(prg.__file__)), "include", "pagerank.h")).read()
     assert int(re.search(r"#define PR_LAYOUT_SLACK (\d+)", hdr).group(1)) == prg.PR_LAYOUT_SLACK
+
+
+def test_run_rejects_mismatched_buffers_before_calling_the_library(monkeypatch):
+    # pr_run reads x_init and writes the ranks through raw pointers, n values of
+    # the run's type, so the binding must refuse any other buffer before the call
+    torch = pytest.importorskip("torch")
+    import numpy as np
+    g = prg.Graph.__new__(prg.Graph)        # no device handle: nothing may reach the library
+    g.n, g.m, g.device, g._h = 10, 0, 0, None
+    calls = []
+    monkeypatch.setattr(prg, "pr_run", lambda *a: calls.append(a))
+    good = np.zeros(10, dtype=np.float32)
+    cases = [
+        dict(out=np.zeros(9, dtype=np.float32)),                 # too short
+        dict(out=np.zeros(11, dtype=np.float32)),                # too long
+        dict(out=np.zeros(10, dtype=np.float64)),                # fp64 buffer, fp32 run
+        dict(out=torch.zeros(10, dtype=torch.float64)),
+        dict(out=np.zeros(20, dtype=np.float32)[::2]),           # not contiguous
+        dict(out=[0.0] * 10),                                    # not an array
+        dict(out=good, x_init=np.zeros(9, dtype=np.float32)),
+        dict(out=good, x_init=torch.zeros(10, dtype=torch.float64)),
+        dict(out=good, x_init=np.zeros(10, dtype=np.float64)),
+        dict(out=np.zeros(10, dtype=np.float32), dtype=torch.float64),
+        dict(out=good, dtype=torch.int32),
+    ]
+    for kw in cases:
+        with pytest.raises((TypeError, ValueError)):
+            g.run(0.85, 1e-6, 10, **kw)
+    assert not calls
