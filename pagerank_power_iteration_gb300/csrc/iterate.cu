@@ -18,9 +18,12 @@
 //     CTA-wide barrier); rows of 33..1024 in-edges are taken 32 consecutive
 //     rows at a time by one warp that streams their int4s flat and forms the
 //     row sums with a segmented scan; rows of 1..32 in-edges one per lane,
-//     sorted by length and stored interleaved by blocks of 32; rows without
-//     in-edges take the constant term only. Every row is padded to whole
-//     16-byte index loads;
+//     sorted by length and stored interleaved by blocks of 32, each warp
+//     reading where its next 32 blocks lie before it starts them; rows
+//     without in-edges take the constant term only. Every row is padded to
+//     whole 16-byte index loads. Each warp takes the three gathering classes
+//     in its own order (starting at class warp % 3), so the classes run side
+//     by side on every SM;
 //   - the combine reads D from device memory (Day 40, "Keep the dangling mass
 //     on the device"), writes s' and accumulates the L1 distance and the next
 //     dangling mass;
