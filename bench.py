@@ -120,17 +120,17 @@ def kernel_source_digest() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per update of k_iterate from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"k_iterate_{workload}.md")
+    """DRAM bytes per update of k_iterate from the committed ncu record
+    profiles/k_iterate_<workload>.json, if it was taken on the current kernel
+    source; else None. Returns (bytes per update, the record)."""
+    path = os.path.join(ROOT, "profiles", f"k_iterate_{workload}.json")
     if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    src = re.search(r"^source_digest:\s*(\w+)", text, re.M)
-    val = re.search(r"^dram_bytes_per_update:\s*([0-9.eE+]+)", text, re.M)
-    if not src or not val or src.group(1) != kernel_source_digest():
-        return None
-    return float(val.group(1))
+        return None, None
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_digest") != kernel_source_digest():
+        return None, None
+    return float(rec["dram_bytes_per_update"]), rec
 
 
 class ClockSampler:
@@ -316,7 +316,7 @@ def run_ours(args, rank, world, local_rank, dist):
     peak, peak_kind = measured_peak_hbm()
     achieved = bm["b_spmv"] / (per_update_ms * 1e-3) / 1e9
     launches = sum(info["build_launches"] + s["launches"] for s in stats)
-    traffic = profiled_traffic(args.workload)
+    traffic, traffic_rec = profiled_traffic(args.workload)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -340,6 +340,10 @@ def run_ours(args, rank, world, local_rank, dist):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
+            "traffic_source": (f"profiles/k_iterate_{args.workload}.json: ncu dram__bytes_read.sum + "
+                               f"dram__bytes_write.sum over {traffic_rec['updates']} updates of "
+                               f"{traffic_rec['workload']}, per update" if traffic_rec else
+                               "null: no ncu record taken on the current kernel source"),
             "kernel": "k_iterate (fused gather SpMV + combine + L1/D reductions, one launch per update)",
             "bytes_per_launch": bm["b_spmv"], "bytes_model": "4(n+1) + 8m + 4n (row_ptr, col_idx, "
             "per-edge gather, y)", "peak_source": f"{peak_kind} hbm_gbs",
@@ -354,7 +358,7 @@ def run_ours(args, rank, world, local_rank, dist):
     # against the random-gather rate of this GPU measured here
     hot = int(info["edges_hot_f32" if args.dtype == "f32" else "edges_hot_f64"])
     l2_gathers = m - hot
-    g_peak = prg.pr_measure_gather_rate(n, dcode, GATHER_PROBE, sp)
+    g_peak = prg.pr_measure_gather_rate(n, dcode, GATHER_PROBE, sp, prg.PR_GATHER_LOAD)
     g_ach = l2_gathers / (per_update_ms * 1e-3)
     line["gather_roofline"] = {
         "bound": "l2 random gather", "achieved": round(g_ach / 1e9, 2),

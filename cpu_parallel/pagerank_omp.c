@@ -1,10 +1,10 @@
 /* Multi-core CPU PageRank: the power iteration as a pull over the in-edge
  * CSR, parallelised with OpenMP over all host cores.
  *
- * A measured baseline that bench.py times beside the GPU path, as the survey
- * of GPU graph-analytics strategies ("A Reproducible Empirical Study of GPU
- * Graph-Analytics Strategies on Irregular Security Graphs") reports its GPU
- * numbers against the full multi-core CPU (its T1 OpenMP tier). It is neither
+ * A measured baseline that bench.py times beside the GPU path, in the way
+ * "A Reproducible Empirical Study of GPU Graph-Analytics Strategies on
+ * Irregular Security Graphs" reports its GPU numbers against the full
+ * multi-core CPU (its T1 OpenMP tier). It is neither
  * the oracle (which
  * stays single-threaded and plain) nor part of the product: the CUDA library
  * never links or calls it, and it shares no code with either.

@@ -25,9 +25,11 @@
  *  - Vertex ids are int32 in [0, n); edge offsets are int64 on input and
  *    int32 inside the library, so 1 <= n <= 2^31 - 2 and 0 <= m <= 2^31 - 1.
  *  - A pointer argument may point to host memory (pageable or pinned) or to
- *    device memory of the current device; the library tells them apart with
- *    cudaPointerGetAttributes and copies as needed. Managed memory is treated
- *    as device memory.
+ *    device memory of the current device (of the graph's device for pr_run);
+ *    the library tells them apart with cudaPointerGetAttributes and copies as
+ *    needed. Managed memory is treated as device memory. Device memory of
+ *    any other GPU is rejected with PR_ERR_INVALID_ARG before any work, since
+ *    a kernel that dereferenced it would make a peer access nobody enabled.
  *  - `stream` is a cudaStream_t passed as void* (for example
  *    torch.cuda.current_stream().cuda_stream); NULL means the legacy default
  *    stream. All device work of a call is ordered on that stream.
@@ -181,11 +183,12 @@ pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
  * array). The pages have no counterpart: this is the library's own
  * single-pass look-back scan (the one pr_graph_create uses for in_ptr)
  * offered to callers that must not call cudaMalloc, such as code running
- * inside a framework that owns all device memory through its own pool, or
- * work issued while another thread captures a CUDA graph in global capture
- * mode, where an allocation would invalidate the capture.
- *   counts   device pointer, `count` int32 values; the total must fit int32
- *   offsets  device pointer, `count + 1` int32 values (caller-owned)
+ * inside a framework that owns all device memory through its own pool and
+ * hands the library only buffers it has already carved out.
+ *   counts   device pointer (memory of the current device), `count` int32
+ *            values, each >= 0, whose total must fit int32
+ *   offsets  device pointer (memory of the current device), `count + 1`
+ *            int32 values (caller-owned)
  *   count    0 <= count <= PR_SCAN_NOALLOC_MAX; larger counts are rejected
  *            with PR_ERR_TOO_LARGE and a message
  * Scratch: the look-back descriptors live in one fixed file-scope device
@@ -197,11 +200,25 @@ pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
  * part it uses, so calls that overlap on the GPU (from two host threads, or
  * on two streams without ordering) race and give wrong results: serialize
  * them. The call synchronizes `stream` and returns PR_OK,
- * PR_ERR_INVALID_ARG (NULL or host pointers, count < 0), PR_ERR_TOO_LARGE,
- * PR_ERR_TIMEOUT or PR_ERR_CUDA. It makes no cudaMalloc or cudaFree call.
+ * PR_ERR_INVALID_ARG (NULL pointers, pointers that are not memory of the
+ * current device, count < 0, or a negative entry in counts, which the kernel
+ * detects), PR_ERR_TOO_LARGE (count beyond the scratch, or a total above
+ * INT32_MAX, which the kernel detects), PR_ERR_TIMEOUT or PR_ERR_CUDA. After
+ * an error that the kernel detected, the contents of offsets are not
+ * meaningful. It makes no cudaMalloc or cudaFree call.
  */
 pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
                                     void *stream);
+
+/* The path a random gather takes (pr_measure_gather_rate). */
+typedef enum pr_gather_path {
+    PR_GATHER_LOAD = 0,         /* ld.global.cg from the warps: the path the update uses */
+    PR_GATHER_TMA = 1,          /* the tensor memory accelerator: cp.async.bulk.tensor
+                                   tile::gather4 copies of four 16-byte rows into shared
+                                   memory, issued by the lanes, completed on mbarriers */
+    PR_GATHER_BOTH = 2          /* both at once, the gathers split between them in the
+                                   ratio of their rates measured alone */
+} pr_gather_path;
 
 /*
  * Measures the current GPU's rate of random gathers: loads of single dtype
@@ -211,20 +228,26 @@ pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int
  * serve (those are m - edges_hot per update, see pr_graph_info), so a run's
  * rate of such gathers can be reported as a fraction of it. The pages have
  * no counterpart: it is the denominator of the update kernel's gather
- * roofline. The indices are drawn on the device (SplitMix64 of the position,
- * reduced mod n) and streamed as int32; the time is that of three passes
- * after a warm-up, taken with CUDA events on `stream`.
+ * roofline, and, with `path`, the measurement of whether a second request
+ * path (the TMA's tile::gather4, which fetches a 16-byte row per gathered
+ * element) adds to the rate of the warps' loads. The indices are drawn on
+ * the device (SplitMix64 of the position, reduced mod n) and streamed as
+ * int32; the time is that of three passes after a warm-up, taken with CUDA
+ * events on `stream`. PR_GATHER_BOTH also measures the two paths alone first.
  *   n             elements of the state vector, 1 <= n <= 2^31 - 2 (pass the
  *                 graph's n to measure at the run's working-set size)
  *   dtype         PR_F32 or PR_F64: the element type gathered
  *   gathers       gathers per pass, 1 <= gathers <= 2^30 (about 2^27 gives a
  *                 pass of a few tenths of a millisecond)
+ *   path          PR_GATHER_LOAD, PR_GATHER_TMA or PR_GATHER_BOTH
  *   gathers_per_s receives the measured rate
- * Allocates n * sizeof(dtype) + 4 * gathers bytes from the library's pool
- * for the duration of the call and synchronizes `stream`. Returns PR_OK,
- * PR_ERR_INVALID_ARG, PR_ERR_OOM or PR_ERR_CUDA.
+ * Allocates about n * sizeof(dtype) + 4 * gathers bytes from the library's
+ * pool for the duration of the call and synchronizes `stream`. Every wait on
+ * a copy is bounded; one that gives up makes the call return PR_ERR_TIMEOUT
+ * (the context stays usable). Returns PR_OK, PR_ERR_INVALID_ARG, PR_ERR_OOM,
+ * PR_ERR_TIMEOUT or PR_ERR_CUDA.
  */
-pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathers,
+pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathers, pr_gather_path path,
                                  double *gathers_per_s, void *stream);
 
 /* Frees the handle and returns all device memory it owns to the library's

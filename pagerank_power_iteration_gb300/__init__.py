@@ -20,10 +20,12 @@ import numpy as np
 __all__ = [
     "PR_OK", "PR_NOT_CONVERGED", "PR_ERR_INVALID_ARG", "PR_ERR_INVALID_GRAPH",
     "PR_ERR_TOO_LARGE", "PR_ERR_OOM", "PR_ERR_CUDA", "PR_ERR_TIMEOUT", "PR_F32", "PR_F64",
+    "PR_GATHER_LOAD", "PR_GATHER_TMA", "PR_GATHER_BOTH",
     "PageRankError", "pr_graph_info", "pr_run_stats", "lib", "library_path",
     "pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info", "pr_graph_last_run",
     "pr_graph_destroy", "pr_last_error", "pr_version", "pr_exclusive_scan_noalloc",
     "pr_measure_gather_rate", "PR_SCAN_NOALLOC_MAX", "PR_LAYOUT_SLACK", "max_edges", "Graph", "EXPORTED_SYMBOLS",
+    "pr_test_fail_alloc_after", "pr_test_pool_used_bytes", "pr_test_scan_timeout",
 ]
 
 PR_OK = 0
@@ -36,10 +38,15 @@ PR_ERR_CUDA = -5
 PR_ERR_TIMEOUT = -6
 PR_F32 = 0
 PR_F64 = 1
+PR_GATHER_LOAD = 0
+PR_GATHER_TMA = 1
+PR_GATHER_BOTH = 2
 
 EXPORTED_SYMBOLS = ("pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info",
                     "pr_graph_last_run", "pr_graph_destroy", "pr_last_error", "pr_version",
-                    "pr_exclusive_scan_noalloc", "pr_measure_gather_rate")
+                    "pr_exclusive_scan_noalloc", "pr_measure_gather_rate",
+                    # test hooks (include/pagerank_testing.h)
+                    "pr_test_fail_alloc_after", "pr_test_pool_used_bytes", "pr_test_scan_timeout")
 PR_SCAN_NOALLOC_MAX = 1 << 26
 PR_LAYOUT_SLACK = 8192
 
@@ -124,8 +131,14 @@ def lib():
         L.pr_version.restype = ctypes.c_char_p
         L.pr_exclusive_scan_noalloc.argtypes = [vp, vp, i64, vp]
         L.pr_exclusive_scan_noalloc.restype = ctypes.c_int
-        L.pr_measure_gather_rate.argtypes = [i64, ctypes.c_int, i64, ctypes.POINTER(dbl), vp]
+        L.pr_measure_gather_rate.argtypes = [i64, ctypes.c_int, i64, ctypes.c_int, ctypes.POINTER(dbl), vp]
         L.pr_measure_gather_rate.restype = ctypes.c_int
+        L.pr_test_fail_alloc_after.argtypes = [i64]
+        L.pr_test_fail_alloc_after.restype = None
+        L.pr_test_pool_used_bytes.argtypes = [ctypes.POINTER(i64)]
+        L.pr_test_pool_used_bytes.restype = ctypes.c_int
+        L.pr_test_scan_timeout.argtypes = [i64, i32, vp]
+        L.pr_test_scan_timeout.restype = ctypes.c_int
         _lib = L
         return L
 
@@ -180,13 +193,34 @@ def pr_exclusive_scan_noalloc(counts: int, offsets: int, count: int, stream: int
     _check(lib().pr_exclusive_scan_noalloc(counts, offsets, count, stream))
 
 
-def pr_measure_gather_rate(n: int, dtype: int, gathers: int, stream: int | None = None) -> float:
+def pr_measure_gather_rate(n: int, dtype: int, gathers: int, stream: int | None = None,
+                           path: int = PR_GATHER_LOAD) -> float:
     """Raw call. Random gathers per second from an n-element state vector of
-    dtype (PR_F32 or PR_F64) on the current GPU: the ceiling of the update's
-    gathers that shared memory does not serve."""
+    dtype (PR_F32 or PR_F64) on the current GPU, through `path`
+    (PR_GATHER_LOAD: the warps' loads, the ceiling of the update's gathers that
+    shared memory does not serve; PR_GATHER_TMA: TMA tile::gather4 copies;
+    PR_GATHER_BOTH: both at once)."""
     rate = ctypes.c_double(0.0)
-    _check(lib().pr_measure_gather_rate(n, dtype, gathers, ctypes.byref(rate), stream))
+    _check(lib().pr_measure_gather_rate(n, dtype, gathers, path, ctypes.byref(rate), stream))
     return rate.value
+
+
+def pr_test_fail_alloc_after(k: int) -> None:
+    """Test hook: the k-th pool allocation from now fails with PR_ERR_OOM (0: off)."""
+    lib().pr_test_fail_alloc_after(int(k))
+
+
+def pr_test_pool_used_bytes() -> int:
+    """Test hook: bytes of the current device's library pool in use (0 if no pool yet)."""
+    used = ctypes.c_int64(0)
+    _check(lib().pr_test_pool_used_bytes(ctypes.byref(used)))
+    return used.value
+
+
+def pr_test_scan_timeout(count: int, spin_limit: int, stream: int | None = None) -> int:
+    """Test hook: a scan whose first tile never publishes. Returns the status
+    (PR_ERR_TIMEOUT when the bounded look-back waits ran out) without raising."""
+    return lib().pr_test_scan_timeout(int(count), int(spin_limit), stream)
 
 
 def pr_last_error() -> str:
@@ -216,9 +250,10 @@ def _ptr(a) -> int | None:
     return a.data_ptr()
 
 
-def _check_vector(a, n: int, dtype, name: str) -> None:
+def _check_vector(a, n: int, dtype, name: str, device: int) -> None:
     """Raises unless ``a`` (numpy array or torch tensor) holds exactly n
-    contiguous values of ``dtype`` (torch.float32 or torch.float64)."""
+    contiguous values of ``dtype`` (torch.float32 or torch.float64), in host
+    memory or on CUDA device ``device``."""
     import torch
     if isinstance(a, np.ndarray):
         want = np.float32 if dtype == torch.float32 else np.float64
@@ -228,6 +263,10 @@ def _check_vector(a, n: int, dtype, name: str) -> None:
     elif isinstance(a, torch.Tensor):
         if a.dtype != dtype:
             raise TypeError(f"{name} must be {dtype}, got {a.dtype}")
+        # host memory, or memory of the graph's own GPU: a kernel must never
+        # be handed another GPU's memory
+        if a.device.type != "cpu" and a.device != torch.device("cuda", device):
+            raise ValueError(f"{name} must be on the CPU or on cuda:{device}, got {a.device}")
         size, contiguous = a.numel(), a.is_contiguous()
     else:
         raise TypeError(f"{name} must be a numpy array or a torch tensor")
@@ -291,9 +330,9 @@ class Graph:
         # the library reads and writes exactly n values of the run's type
         # through these pointers, so a shorter buffer or another type would be
         # read or written out of bounds
-        _check_vector(out, self.n, dtype, "out")
+        _check_vector(out, self.n, dtype, "out", self.device)
         if x_init is not None:
-            _check_vector(x_init, self.n, dtype, "x_init")
+            _check_vector(x_init, self.n, dtype, "x_init", self.device)
         st, it, l1 = pr_run(self._h, float(d), float(tol), int(max_iter), code, _ptr(out),
                             _ptr(x_init), _stream(stream))
         return out, it, l1, st == PR_OK

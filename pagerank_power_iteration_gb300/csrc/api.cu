@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -39,10 +40,13 @@ pr_status cuda_status(cudaError_t e, const char *what)
 // graph built after another one was destroyed reuses its memory instead of
 // paying cudaMalloc and cudaFree (which synchronises the device) again. The
 // pool holds its peak size until the process exits.
+static std::mutex g_pool_mu;
+static cudaMemPool_t g_pools[kMaxDevices] = {};
+
 static pr_status device_pool(cudaMemPool_t *out)
 {
-    static std::mutex mu;
-    static cudaMemPool_t pools[kMaxDevices] = {};
+    std::mutex &mu = g_pool_mu;
+    cudaMemPool_t *pools = g_pools;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -69,10 +73,54 @@ static pr_status device_pool(cudaMemPool_t *out)
     return PR_OK;
 }
 
+// Test hook: the k-th pool allocation from now fails (0: none does).
+static std::atomic<int64_t> g_fail_countdown{0};
+
+void fail_alloc_after(int64_t k) { g_fail_countdown.store(k > 0 ? k : 0); }
+
+pr_status pool_used_bytes(int64_t *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(PR_ERR_CUDA, "device ordinal %d out of range", dev);
+    // frees are stream ordered: let every pending one reach the pool
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaDeviceSynchronize");
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lock(g_pool_mu);
+        pool = g_pools[dev];
+    }
+    if (pool == nullptr) {   // never created: nothing allocated
+        *out = 0;
+        return PR_OK;
+    }
+    uint64_t used = 0;
+    e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &used);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaMemPoolGetAttribute");
+    *out = (int64_t)used;
+    return PR_OK;
+}
+
 pr_status pool_alloc(void **p, size_t bytes, cudaStream_t s)
 {
     if (bytes == 0)
         bytes = 16;
+    for (int64_t k = g_fail_countdown.load(); k > 0; k = g_fail_countdown.load()) {
+        if (g_fail_countdown.compare_exchange_weak(k, k - 1)) {
+            if (k == 1) {
+                *p = nullptr;
+                return set_error(PR_ERR_OOM, "device allocation of %zu bytes failed (injected by "
+                                             "pr_test_fail_alloc_after)", bytes);
+            }
+            break;
+        }
+    }
     cudaMemPool_t pool;
     pr_status st = device_pool(&pool);
     if (st != PR_OK)
@@ -103,15 +151,19 @@ pr_status graph_alloc(pr_graph *g, void **p, size_t bytes, cudaStream_t s)
     return PR_OK;
 }
 
-bool is_device_pointer(const void *p)
+PtrKind pointer_kind(const void *p, int device)
 {
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return kPtrHost;
     }
-    return attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged;
+    if (attr.type == cudaMemoryTypeManaged)
+        return kPtrDevice;
+    if (attr.type == cudaMemoryTypeDevice)
+        return attr.device == device ? kPtrDevice : kPtrOtherDevice;
+    return kPtrHost;
 }
 
 }  // namespace prk
@@ -223,8 +275,15 @@ PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
         if (e != cudaSuccess) { st = prk::cuda_status(e, "memset"); break; }
 
         // inputs on the device (borrowed, or staged copies freed below)
-        const bool rp_dev = prk::is_device_pointer(row_ptr);
-        const bool ci_dev = (m == 0) || prk::is_device_pointer(col_idx);
+        const prk::PtrKind rp_kind = prk::pointer_kind(row_ptr, dev);
+        const prk::PtrKind ci_kind = m == 0 ? prk::kPtrDevice : prk::pointer_kind(col_idx, dev);
+        if (rp_kind == prk::kPtrOtherDevice || ci_kind == prk::kPtrOtherDevice) {
+            st = set_error(PR_ERR_INVALID_ARG, "row_ptr and col_idx must be host memory or memory of "
+                                               "the current device (%d)", dev);
+            break;
+        }
+        const bool rp_dev = rp_kind == prk::kPtrDevice;
+        const bool ci_dev = ci_kind == prk::kPtrDevice;
         int64_t ends[2];
         if (rp_dev) {
             e = cudaMemcpyAsync(&ends[0], row_ptr, sizeof(int64_t), cudaMemcpyDeviceToHost, s);
@@ -343,9 +402,11 @@ PR_API pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info)
     return PR_OK;
 }
 
-PR_API pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathers,
+PR_API pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathers, pr_gather_path path,
                                         double *gathers_per_s, void *stream)
 {
+    if (path != PR_GATHER_LOAD && path != PR_GATHER_TMA && path != PR_GATHER_BOTH)
+        return set_error(PR_ERR_INVALID_ARG, "unknown gather path %d", (int)path);
     if (gathers_per_s == nullptr)
         return set_error(PR_ERR_INVALID_ARG, "gathers_per_s is NULL");
     if (n < 1 || n > kMaxN)
@@ -355,7 +416,7 @@ PR_API pr_status pr_measure_gather_rate(int64_t n, pr_dtype dtype, int64_t gathe
                          (long long)gathers);
     if (dtype != PR_F32 && dtype != PR_F64)
         return set_error(PR_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    return prk::measure_gather_rate(n, (int)dtype, gathers, gathers_per_s, (cudaStream_t)stream);
+    return prk::measure_gather_rate(n, (int)dtype, gathers, (int)path, gathers_per_s, (cudaStream_t)stream);
 }
 
 PR_API pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats)
@@ -378,6 +439,20 @@ PR_API pr_status pr_exclusive_scan_noalloc(const int32_t *counts, int32_t *offse
                                            void *stream)
 {
     return prk::exclusive_scan_noalloc(counts, offsets, count, (cudaStream_t)stream);
+}
+
+PR_API void pr_test_fail_alloc_after(int64_t k) { prk::fail_alloc_after(k); }
+
+PR_API pr_status pr_test_pool_used_bytes(int64_t *used)
+{
+    if (used == nullptr)
+        return set_error(PR_ERR_INVALID_ARG, "used is NULL");
+    return prk::pool_used_bytes(used);
+}
+
+PR_API pr_status pr_test_scan_timeout(int64_t count, int32_t spin_limit, void *stream)
+{
+    return prk::scan_timeout_probe(count, spin_limit, (cudaStream_t)stream);
 }
 
 PR_API const char *pr_last_error(void) { return prk::g_last_error; }

@@ -65,10 +65,21 @@ struct IterArgs {
     const int32_t *w_split;   // [warps + 1]: warp-class rows of each warp of the grid
     int64_t n, n_c, n_w, n_t, n_z, n_chunks;
     int64_t t_short;          // first thread-class block whose rows span at most two int4s
+    int rotate;               // 1: warp w starts at gather class w % 3
 };
 
 // streaming (evict-first) loads of the index stream
 __device__ __forceinline__ int4 ld_stream4(const int4 *p) { return __ldcs(p); }
+
+// Asynchronous 16-byte global -> shared copies (cp.async, L2 only), their
+// commit, and the wait for all of this thread's outstanding ones.
+__device__ __forceinline__ void cp_async16(int4 *smem_dst, const int4 *gmem_src)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v)
@@ -399,44 +410,62 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     const T d = T(dd);
     const T base = T((1.0 - dd) * inv_n + dd * D * inv_n);
 
-    // the head of the state vector, where the work order puts the most
-    // gathered vertices, staged in shared memory for this update
-    // (16-byte copies, all of a thread's loads in flight before its stores;
-    // both buffers are 16-byte aligned)
+    unsigned long long l1 = 0ull, dm = 0ull;   // fixed point, see to_fixed
+
+    // The head of the state vector, where the work order puts the most
+    // gathered vertices, is staged in shared memory for this update with
+    // asynchronous 16-byte copies (cp.async; both buffers are 16-byte
+    // aligned). The rows without in-edges, which gather nothing, are combined
+    // while the copies land.
     T *s_hot = reinterpret_cast<T *>(s_dyn);
     {
-        constexpr int kPer = (kHotBytes / 16 + kIterBlock - 1) / kIterBlock;
         const int32_t hot4 = (int32_t)((int64_t)hot * (int64_t)sizeof(T) / 16);
         const int4 *src = reinterpret_cast<const int4 *>(s_old);
         int4 *dst = reinterpret_cast<int4 *>(s_hot);
-        int4 v[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k)
-            if (tid + k * kIterBlock < hot4)
-                v[k] = __ldcg(src + tid + k * kIterBlock);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k)
-            if (tid + k * kIterBlock < hot4)
-                dst[tid + k * kIterBlock] = v[k];
+        for (int32_t q = tid; q < hot4; q += kIterBlock)
+            cp_async16(dst + q, src + q);
+        cp_async_commit();
         for (int32_t u = (int32_t)(hot4 * 16 / (int32_t)sizeof(T)) + tid; u < hot; u += kIterBlock)
             s_hot[u] = s_old[u];
     }
+
+    // rows without in-edges: x' = base; eight rows per thread in flight
+    {
+        const int64_t z0 = a.n - a.n_z, stride = G * kIterBlock;
+        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < a.n; i += 8 * stride) {
+            int32_t dg[8];
+            T so[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (i + t * stride < a.n) {
+                    dg[t] = a.w_deg[i + t * stride];
+                    so[t] = s_old[i + t * stride];
+                }
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (i + t * stride < a.n)
+                    combine_row(i + t * stride, T(0), dg[t], so[t], s_new, base, d, l1, dm);
+        }
+    }
+    cp_async_wait_all();
     __syncthreads();
     const Gather<T> gat{s_old, s_hot, hot};
 
-    unsigned long long l1 = 0ull, dm = 0ull;   // fixed point, see to_fixed
-
+    // Work ranges are numbered warp-major across the grid (gw = warp * G +
+    // CTA), so the 32 warps of a CTA take ranges spread evenly over each
+    // class instead of 32 neighbouring ones: rows at the head of a class cost
+    // more than rows at its tail, and every CTA gets the same mix.
+    //
     // CTA class: rows with more than 1024 in-edges, cut into chunks of
     // kChunkEdges (whole int4s). Warp gw streams the contiguous chunk range
-    // [gw * per, (gw + 1) * per), so a CTA streams 32 consecutive ranges of
-    // the hub edges. A warp sums each row's chunks in its range in registers;
-    // a row that lies wholly in the range is combined at once. A row that
+    // [gw * per, (gw + 1) * per). A warp sums each row's chunks in its range
+    // in registers; a row that lies wholly in the range is combined at once. A row that
     // crosses a range boundary is handed off: each warp stores its piece's
     // sum at the piece's first chunk (the row's first chunk, or a multiple of
     // `per`), adds its chunk count to the row's arrival counter, and the warp
     // that completes the count adds the pieces in chunk order and combines
     // the row. No CTA-wide barrier, and no wait.
-    const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t gw = (int64_t)warp * G + blockIdx.x;
     const int4 *cv = reinterpret_cast<const int4 *>(a.w_col);
     auto phase_hub = [&]() {
         const int64_t nwarps = G * kWarps;
@@ -571,14 +600,16 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
             }
         }
     };
-    // Each warp takes the three gather phases in its own order: warp w of the
-    // CTA starts with phase w % 3 (hub, warp-class, thread-class) and wraps
-    // around. Every SM then runs all three at once, and the thread class,
-    // whose short rows leave few gathers in flight per warp, overlaps the
-    // streaming classes instead of running alone at the end of the update.
-    // What a warp computes does not depend on the order (no phase waits on
-    // another, and the L1 and D totals are exact), so results are unchanged.
-    const int rot = warp % 3;
+    // On graphs with many rows, each warp takes the three gather phases in
+    // its own order: warp w of the CTA starts with phase w % 3 (hub,
+    // warp-class, thread-class) and wraps around. Every SM then runs all
+    // three at once, and the thread class, whose short rows leave few gathers
+    // in flight per warp, overlaps the streaming classes instead of running
+    // alone at the end of the update. On small graphs (a.rotate == 0), which
+    // sit in L2 and are bound by fixed costs, every warp takes the classes in
+    // one order. What a warp computes does not depend on the order (no phase
+    // waits on another, and the L1 and D totals are exact).
+    const int rot = a.rotate ? warp % 3 : 0;
     if (rot == 0) {
         phase_hub();
         phase_warp();
@@ -591,25 +622,6 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         phase_thread();
         phase_hub();
         phase_warp();
-    }
-
-    // rows without in-edges: x' = base; eight rows per thread in flight
-    {
-        const int64_t z0 = a.n - a.n_z, stride = G * kIterBlock;
-        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < a.n; i += 8 * stride) {
-            int32_t dg[8];
-            T so[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-                if (i + t * stride < a.n) {
-                    dg[t] = a.w_deg[i + t * stride];
-                    so[t] = s_old[i + t * stride];
-                }
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-                if (i + t * stride < a.n)
-                    combine_row(i + t * stride, T(0), dg[t], so[t], s_new, base, d, l1, dm);
-        }
     }
 
     // reductions: one fp64 partial pair per CTA, the last CTA sums them
@@ -770,17 +782,40 @@ IterArgs<T> make_args(pr_graph *g)
     a.n_z = g->n_z;
     a.n_chunks = g->n_chunks;
     a.t_short = g->t_short;
+    a.rotate = (g->n - g->n_z >= kRotateRows) ? 1 : 0;
     return a;
 }
 
 // Allocates a precision's state and builds its graph: one conditional WHILE
 // node whose body is one k_iterate launch.
 template <typename T>
+pr_status prepare_once(pr_graph *g, cudaStream_t s);
+
+// prepare_once, undone on failure: the blocks it took from the pool go back
+// and the handle is as before, so a later pr_run can try again.
+template <typename T>
 pr_status prepare(pr_graph *g, cudaStream_t s)
 {
     DtypeState &st = g->st[sizeof(T) == 8 ? 1 : 0];
     if (st.ready)
         return PR_OK;
+    const size_t n_allocs = g->allocs.size();
+    const int64_t bytes = g->device_bytes;
+    const pr_status r = prepare_once<T>(g, s);
+    if (r != PR_OK) {
+        for (size_t k = n_allocs; k < g->allocs.size(); ++k)
+            pool_free(g->allocs[k], s);
+        g->allocs.resize(n_allocs);
+        g->device_bytes = bytes;
+        st = DtypeState();
+    }
+    return r;
+}
+
+template <typename T>
+pr_status prepare_once(pr_graph *g, cudaStream_t s)
+{
+    DtypeState &st = g->st[sizeof(T) == 8 ? 1 : 0];
     pr_status r;
     const int64_t hot_cap = kHotBytes / (int64_t)sizeof(T);
     st.hot = (int32_t)(g->n + 1 < hot_cap ? g->n + 1 : hot_cap);
@@ -864,6 +899,13 @@ template <typename T>
 pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *ranks_out,
                     const void *x_init, int32_t *iters_out, double *l1_out, cudaStream_t s)
 {
+    // the caller's buffers: host memory, or memory the graph's device may
+    // dereference; memory of another GPU is refused before any work
+    const PtrKind out_kind = pointer_kind(ranks_out, g->device);
+    const PtrKind xi_kind = x_init ? pointer_kind(x_init, g->device) : kPtrHost;
+    if (out_kind == kPtrOtherDevice || xi_kind == kPtrOtherDevice)
+        return set_error(PR_ERR_INVALID_ARG, "ranks_out and x_init must be host memory or memory of "
+                                             "the graph's device (%d)", g->device);
     pr_status r = prepare<T>(g, s);
     if (r != PR_OK)
         return r;
@@ -874,7 +916,7 @@ pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *r
 
     const T *xi = nullptr;
     if (x_init) {
-        if (is_device_pointer(x_init)) {
+        if (xi_kind == kPtrDevice) {
             xi = (const T *)x_init;
         } else {
             e = cudaMemcpyAsync(st.stage, x_init, bytes, cudaMemcpyHostToDevice, s);
@@ -883,7 +925,7 @@ pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *r
             xi = (const T *)st.stage;
         }
     }
-    const bool out_dev = is_device_pointer(ranks_out);
+    const bool out_dev = out_kind == kPtrDevice;
     T *out = out_dev ? (T *)ranks_out : (T *)st.stage;
 
     e = cudaEventRecord(g->ev[0], s);

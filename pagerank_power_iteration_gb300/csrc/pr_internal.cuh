@@ -31,6 +31,10 @@ constexpr int32_t kHotF64 = kHotBytes / 8;   // and fp64 runs
 // per-row work small: a pure edge balance (0) measured best (RMAT-24 update
 // 0.754 ms at 32, 0.735 at 16, 0.711 at 0).
 constexpr int kWarpRowCost = 0;
+// Graphs with fewer rows that have in-edges than this take the gather
+// classes in one order in every warp (small graphs sit in L2 and are bound
+// by fixed costs); larger ones start each warp at its own class.
+constexpr int64_t kRotateRows = (int64_t)1 << 20;
 // Work-CSR entry that pads a row to whole 16-byte loads; it gathers 0. (A
 // pad pointing at a zero slot of the state instead makes every pad of every
 // SM read one L2 line, a hot spot that was measured to cost 15 %.)
@@ -43,6 +47,8 @@ enum : unsigned {
     kErrRowPtr = 1u,    // row_ptr decreases somewhere
     kErrColIdx = 2u,    // a col_idx entry is outside [0, n)
     kErrTimeout = 4u,   // a bounded look-back wait gave up
+    kErrNegative = 8u,  // a scanned count was negative (counted as 0)
+    kErrOverflow = 16u, // a scan's total exceeds INT32_MAX
 };
 
 // Device-resident scalars of a run. Written by the init kernel, read at the
@@ -142,8 +148,12 @@ pr_status pool_alloc(void **p, size_t bytes, cudaStream_t s);
 void pool_free(void *p, cudaStream_t s);
 pr_status graph_alloc(pr_graph *g, void **p, size_t bytes, cudaStream_t s);
 
-// True if p can be dereferenced by the current device as device memory.
-bool is_device_pointer(const void *p);
+// Where a caller's pointer lives, seen from `device`: host memory (pageable
+// or pinned), device memory that `device`'s kernels may dereference (its own
+// memory, or managed memory), or memory of another GPU, which a kernel on
+// `device` must not touch (that would be a peer access nobody enabled).
+enum PtrKind : int { kPtrHost = 0, kPtrDevice = 1, kPtrOtherDevice = 2 };
+PtrKind pointer_kind(const void *p, int device);
 
 // Transpose + classification (transpose.cu). d_row_ptr/d_col are device pointers.
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col,
@@ -152,10 +162,18 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
 // Allocation-free exclusive scan (transpose.cu).
 pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
                                  cudaStream_t s);
+
+// Test hooks (api.cu, transpose.cu): make the k-th pool allocation from now
+// fail with PR_ERR_OOM (k = 0: never); bytes of the current device's pool in
+// use; a scan whose first tile never publishes, so its look-back waits run
+// out after spin_limit polls.
+void fail_alloc_after(int64_t k);
+pr_status pool_used_bytes(int64_t *out);
+pr_status scan_timeout_probe(int64_t count, int spin_limit, cudaStream_t s);
 constexpr int kMaxDevices = 64;
 
 // Random-gather rate of the current GPU (calibrate.cu).
-pr_status measure_gather_rate(int64_t n, int dtype, int64_t gathers, double *rate, cudaStream_t s);
+pr_status measure_gather_rate(int64_t n, int dtype, int64_t gathers, int path, double *rate, cudaStream_t s);
 
 // Iteration (iterate.cu).
 pr_status run(pr_graph *g, double d, double tol, int32_t max_iter, int dtype,

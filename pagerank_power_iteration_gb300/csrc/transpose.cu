@@ -74,14 +74,16 @@ __device__ __forceinline__ void store_desc(unsigned long long *p, unsigned long 
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Waits (bounded) for a published descriptor; returns 0 on timeout. Polls
-// back to back first (the predecessor is usually moments away), then backs off.
-__device__ __forceinline__ unsigned long long wait_desc(const unsigned long long *p, unsigned *err)
+// Waits (bounded: at most spin_limit polls) for a published descriptor;
+// returns 0 on timeout. Polls back to back first (the predecessor is usually
+// moments away), then backs off.
+__device__ __forceinline__ unsigned long long wait_desc(const unsigned long long *p, unsigned *err,
+                                                        int spin_limit)
 {
     unsigned long long v = load_desc(p);
     int spins = 0;
     while ((v >> 62) == 0) {
-        if (++spins > kSpinLimit) {
+        if (++spins > spin_limit) {
             atomicOr(err, kErrTimeout);
             return 0;
         }
@@ -98,7 +100,7 @@ __device__ __forceinline__ unsigned long long wait_desc(const unsigned long long
 // costs a quarter of the round trips; a descriptor still unpublished is
 // waited for (bounded) before it is used.
 __device__ long long look_back(const unsigned long long *desc, int64_t tile, int64_t stride,
-                               unsigned *err)
+                               unsigned *err, int spin_limit)
 {
     long long prefix = 0;
     int64_t p = tile - 1;
@@ -112,7 +114,7 @@ __device__ long long look_back(const unsigned long long *desc, int64_t tile, int
             if (p - k < 0)
                 return prefix;
             if ((v[k] >> 62) == 0) {
-                v[k] = wait_desc(desc + (p - k) * stride, err);
+                v[k] = wait_desc(desc + (p - k) * stride, err, spin_limit);
                 if (v[k] == 0)
                     return prefix;   // timed out: error already flagged
             }
@@ -604,11 +606,15 @@ struct LoadChunkCount {   // number of edge chunks of work row i
 
 // out[i] = sum of load(k) for k < i, for i in [0, count]; out[count] is the
 // total. Single pass: tiles are taken in launch order from a counter and each
-// finds its prefix by decoupled look-back over its predecessors' descriptors.
+// finds its prefix by decoupled look-back over its predecessors' descriptors
+// (each wait at most spin_limit polls). A negative count is added as 0 and
+// sets kErrNegative; a total above INT32_MAX sets kErrOverflow (the offsets
+// are then not meaningful). Both keep every descriptor a valid non-negative
+// sum below 2^62, so the look-back stays well formed.
 template <class Load>
 __global__ void __launch_bounds__(kBlock)
 k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
-            unsigned long long *desc, unsigned *tile_counter, unsigned *err)
+            unsigned long long *desc, unsigned *tile_counter, unsigned *err, int spin_limit)
 {
     __shared__ int32_t s_items[kScanTile + kScanTile / 32];   // padded: no bank conflicts
     __shared__ long long s_warp[kBlock / 32];
@@ -623,10 +629,24 @@ k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
     const int64_t base = tile * kScanTile;
     auto pad = [](int i) { return i + (i >> 5); };
 
-    for (int k = 0; k < kScanItems; ++k) {
-        const int64_t i = base + (int64_t)k * kBlock + tid;
-        s_items[pad(k * kBlock + tid)] = (i < count) ? load(i) : 0;
+    // every load of the thread in flight before the first store (the loads
+    // of the work layout's scans are dependent gathers)
+    bool negative = false;
+    {
+        int32_t ld[kScanItems];
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            const int64_t i = base + (int64_t)k * kBlock + tid;
+            ld[k] = (i < count) ? load(i) : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            negative |= ld[k] < 0;
+            s_items[pad(k * kBlock + tid)] = max(ld[k], 0);
+        }
     }
+    if (negative)
+        atomicOr(err, kErrNegative);
     __syncthreads();
 
     int32_t v[kScanItems];
@@ -654,12 +674,15 @@ k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
             store_desc(desc, kFlagP | (unsigned long long)total);
         } else {
             store_desc(desc + tile, kFlagA | (unsigned long long)total);
-            prefix = look_back(desc, tile, 1, err);
+            prefix = look_back(desc, tile, 1, err, spin_limit);
             store_desc(desc + tile, kFlagP | (unsigned long long)(prefix + total));
         }
         s_prefix = prefix;
-        if (base + kScanTile >= count)   // the last tile writes the total
+        if (base + kScanTile >= count) {   // the last tile writes the total
             out[count] = (int32_t)(prefix + total);
+            if (prefix + total > (long long)INT32_MAX)
+                atomicOr(err, kErrOverflow);
+        }
     }
     __syncthreads();
     long long run = s_prefix + thread_excl;
@@ -738,23 +761,28 @@ __global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *
 // sits at w_ptr[r0] / 4 + k * cnt + j, so that the lanes of a warp, one row
 // each, read consecutive int4s.
 //
-// The kernel also counts the edges whose relabelled source falls in the head
-// of the state vector that the update keeps in shared memory, for fp32
-// (kHotF32 vertices) and fp64 (kHotF64) runs: hot[0] and hot[1] (zeroed by
-// the caller).
-__global__ void __launch_bounds__(kBlock)
+// The kernel also counts, for reporting, the true in-edges of the CTA, warp
+// and thread classes (class_edges[0..2]) and the edges whose relabelled
+// source falls in the head of the state vector that the update keeps in
+// shared memory, for fp32 (kHotF32 vertices) and fp64 (kHotF64) runs: hot[0]
+// and hot[1]. All five counters are zeroed by the caller. Each thread counts
+// the entries it writes in 32 bits (a thread writes far fewer than 2^32 of
+// the m < 2^31 entries); the kernel is held to 32 registers, because the
+// perm gathers need every warp an SM can hold in flight (8 CTAs per SM).
+__global__ void __launch_bounds__(kBlock, 8)
 k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t rows_end,
           const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_first,
           const int32_t *__restrict__ w_ptr, const int32_t *__restrict__ order,
           const int32_t *__restrict__ perm, const int32_t *__restrict__ in_ptr,
           const int32_t *__restrict__ in_col, int32_t *__restrict__ w_col,
-          unsigned long long *__restrict__ hot)
+          unsigned long long *__restrict__ class_edges, unsigned long long *__restrict__ hot)
 {
     const int lane = threadIdx.x & 31;
     const int64_t gtid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
     const int64_t gwarp = gtid >> 5, nwarps = nthreads >> 5;
-    unsigned long long h32 = 0, h64 = 0;
+    unsigned h32 = 0, h64 = 0;             // entries with a hot source
+    unsigned e_cta = 0, e_warp = 0, e_thr = 0;   // true entries written, per class
     auto relabel = [&](int32_t u) {
         const int32_t w = perm[u];
         h32 += (w < kHotF32);
@@ -768,36 +796,60 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
         const int32_t dst = w_ptr[r], len = w_ptr[r + 1] - dst;
         const int32_t k0 = (int32_t)(c - chunk_first[r]) * kChunkEdges;
         const int32_t k1 = min(k0 + kChunkEdges, len);
-        for (int32_t k = k0 + lane; k < k1; k += 32)
+        for (int32_t k = k0 + lane; k < k1; k += 32) {
+            e_cta += (k < deg);
             w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
+        }
     }
     for (int64_t i = n_c + gwarp; i < wide_end; i += nwarps) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
-        for (int32_t k = lane; k < len; k += 32)
+        for (int32_t k = lane; k < len; k += 32) {
+            e_warp += (k < deg);
             w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
+        }
     }
+    // thread-class rows: one thread per row, whole int4s, so the 32 lanes of
+    // a warp (the 32 rows of one block) store 32 consecutive int4s
+    int4 *w_col4 = reinterpret_cast<int4 *>(w_col);
     for (int64_t i = wide_end + gtid; i < rows_end; i += nthreads) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int64_t r0 = wide_end + ((i - wide_end) & ~(int64_t)31);
         const int64_t cnt = min((int64_t)32, rows_end - r0);
         const int64_t j = i - r0;
-        const int64_t blk = w_ptr[r0];
-        const int32_t len = w_ptr[i + 1] - w_ptr[i];
-        for (int32_t k = 0; k < len; ++k)
-            w_col[blk + 4 * ((k >> 2) * cnt + j) + (k & 3)] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
+        const int64_t blk4 = w_ptr[r0] >> 2;   // rows start 16-byte aligned
+        const int32_t len4 = (w_ptr[i + 1] - w_ptr[i]) >> 2;
+        e_thr += (unsigned)deg;
+        for (int32_t q = 0; q < len4; ++q) {
+            const int32_t k = 4 * q;
+            int4 e;
+            e.x = (k + 0 < deg) ? relabel(in_col[src + k + 0]) : kPadSource;
+            e.y = (k + 1 < deg) ? relabel(in_col[src + k + 1]) : kPadSource;
+            e.z = (k + 2 < deg) ? relabel(in_col[src + k + 2]) : kPadSource;
+            e.w = (k + 3 < deg) ? relabel(in_col[src + k + 3]) : kPadSource;
+            w_col4[blk4 + (int64_t)q * cnt + j] = e;
+        }
     }
+    // per CTA: 32-bit warp sums (a warp writes far fewer than 2^32 entries),
+    // 64-bit CTA sums, one atomic per counter and CTA
+    __shared__ unsigned long long s_cnt[5];
+    if (threadIdx.x < 5)
+        s_cnt[threadIdx.x] = 0ull;
+    __syncthreads();
+    unsigned v[5] = {h32, h64, e_cta, e_warp, e_thr};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        h32 += __shfl_xor_sync(0xffffffffu, h32, o);
-        h64 += __shfl_xor_sync(0xffffffffu, h64, o);
+    for (int q = 0; q < 5; ++q) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+        if (lane == 0 && v[q])
+            atomicAdd(&s_cnt[q], (unsigned long long)v[q]);
     }
-    if (lane == 0 && h32) {
-        atomicAdd(hot, h32);
-        atomicAdd(hot + 1, h64);
-    }
+    __syncthreads();
+    if (threadIdx.x < 5 && s_cnt[threadIdx.x])
+        atomicAdd(threadIdx.x < 2 ? hot + threadIdx.x : class_edges + (threadIdx.x - 2), s_cnt[threadIdx.x]);
 }
 
 // First thread-class block (32 work rows from t_begin) whose rows span at
@@ -825,26 +877,6 @@ __global__ void k_permute_deg(int64_t n, const int32_t *__restrict__ order,
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
         w_deg[i] = deg_out[order[i]];
-}
-
-// True in-edges of the CTA, warp and thread classes (work ranges [0, a),
-// [a, b), [b, c)), for reporting.
-__global__ void k_class_edges(int64_t c_end, int64_t a, int64_t b, const int32_t *__restrict__ in_ptr,
-                              const int32_t *__restrict__ order, unsigned long long *out)
-{
-    unsigned long long s[3] = {0, 0, 0};
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < c_end;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int32_t v = order[i];
-        s[i < a ? 0 : i < b ? 1 : 2] += (unsigned long long)(in_ptr[v + 1] - in_ptr[v]);
-    }
-    for (int q = 0; q < 3; ++q) {
-        unsigned long long t = s[q];
-        for (int o = 16; o > 0; o >>= 1)
-            t += __shfl_xor_sync(0xffffffffu, t, o);
-        if ((threadIdx.x & 31) == 0 && t)
-            atomicAdd(out + q, t);
-    }
 }
 
 __global__ void k_fill_chunks(int64_t n_c, int64_t n_chunks, const int32_t *__restrict__ chunk_first,
@@ -902,7 +934,7 @@ pr_status launch_scan(Load load, int32_t *out, int64_t count, unsigned long long
         e = cudaMemsetAsync(counter, 0, sizeof(unsigned), s);
     if (e != cudaSuccess)
         return cuda_status(e, "scan state reset");
-    k_scan_excl<Load><<<(unsigned)tiles, kBlock, 0, s>>>(load, out, count, desc, counter, err);
+    k_scan_excl<Load><<<(unsigned)tiles, kBlock, 0, s>>>(load, out, count, desc, counter, err, kSpinLimit);
     ++*launches;
     e = cudaGetLastError();
     return e == cudaSuccess ? PR_OK : cuda_status(e, "k_scan_excl launch");
@@ -999,8 +1031,13 @@ pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_
                          (long long)count, (long long)kNoAllocScanMax);
     if (offsets == nullptr || (count > 0 && counts == nullptr))
         return set_error(PR_ERR_INVALID_ARG, "NULL pointer");
-    if (!is_device_pointer(offsets) || (count > 0 && !is_device_pointer(counts)))
-        return set_error(PR_ERR_INVALID_ARG, "counts and offsets must be device memory");
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess)
+        return cuda_status(de, "cudaGetDevice");
+    if (pointer_kind(offsets, dev) != kPtrDevice || (count > 0 && pointer_kind(counts, dev) != kPtrDevice))
+        return set_error(PR_ERR_INVALID_ARG, "counts and offsets must be memory of the current device (%d)",
+                         dev);
     unsigned long long *scratch = nullptr;
     pr_status st = noalloc_scratch(&scratch);
     if (st != PR_OK)
@@ -1024,7 +1061,7 @@ pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_
     if (e != cudaSuccess)
         return cuda_status(e, "clearing the scan scratch");
     k_scan_excl<LoadCount><<<(unsigned)tiles, kBlock, 0, s>>>(LoadCount{counts}, offsets, count, desc,
-                                                             counter, err);
+                                                             counter, err, kSpinLimit);
     e = cudaGetLastError();
     unsigned herr = 0;
     if (e == cudaSuccess)
@@ -1035,11 +1072,58 @@ pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_
         return cuda_status(e, "pr_exclusive_scan_noalloc");
     if (herr & kErrTimeout)
         return set_error(PR_ERR_TIMEOUT, "a look-back wait in the scan gave up");
+    if (herr & kErrNegative)
+        return set_error(PR_ERR_INVALID_ARG, "counts has a negative entry (offsets are not valid)");
+    if (herr & kErrOverflow)
+        return set_error(PR_ERR_TOO_LARGE, "the sum of counts exceeds INT32_MAX (offsets are not valid)");
     return PR_OK;
 }
 
-namespace {
-}  // namespace
+pr_status scan_timeout_probe(int64_t count, int spin_limit, cudaStream_t s)
+{
+    if (count <= kScanTile || count > ((int64_t)1 << 24))
+        return set_error(PR_ERR_INVALID_ARG, "count must be in (%d, 2^24] (got %lld)", kScanTile,
+                         (long long)count);
+    if (spin_limit < 1 || spin_limit > (1 << 20))
+        return set_error(PR_ERR_INVALID_ARG, "spin_limit must be in [1, 2^20] (got %d)", spin_limit);
+    const int64_t tiles = (count + kScanTile - 1) / kScanTile;
+    Scratch tmp(s);
+    int32_t *counts = nullptr, *out = nullptr;
+    unsigned long long *desc = nullptr;
+    unsigned *words = nullptr;   // [0] tile counter, [1] error word
+    pr_status st;
+    if ((st = tmp.alloc((void **)&counts, (size_t)count * sizeof(int32_t))) != PR_OK ||
+        (st = tmp.alloc((void **)&out, (size_t)(count + 1) * sizeof(int32_t))) != PR_OK ||
+        (st = tmp.alloc((void **)&desc, (size_t)tiles * sizeof(unsigned long long))) != PR_OK ||
+        (st = tmp.alloc((void **)&words, 2 * sizeof(unsigned))) != PR_OK)
+        return st;
+    // tile 0 never runs: its descriptor stays unpublished, so tile 1 (and
+    // any tile that walks back to it) waits until its spin limit runs out.
+    // Every CTA still reads and writes only inside the buffers above.
+    const unsigned first_tile = 1;
+    cudaError_t e = cudaMemsetAsync(counts, 0, (size_t)count * sizeof(int32_t), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(desc, 0, (size_t)tiles * sizeof(unsigned long long), s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(words, 0, 2 * sizeof(unsigned), s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(words, &first_tile, sizeof(unsigned), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) {
+        k_scan_excl<LoadCount><<<(unsigned)(tiles - 1), kBlock, 0, s>>>(LoadCount{counts}, out, count, desc,
+                                                                        words, words + 1, spin_limit);
+        e = cudaGetLastError();
+    }
+    unsigned herr = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&herr, words + 1, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_status(e, "scan timeout probe");
+    if (herr & kErrTimeout)
+        return set_error(PR_ERR_TIMEOUT, "a look-back wait in the scan gave up");
+    return PR_OK;
+}
 
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, cudaStream_t s)
 {
@@ -1234,18 +1318,12 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         k_relabel<<<g->num_sms * 8, kBlock, 0, s>>>(n, g->n_c, g->n_chunks, g->n_c + g->n_w,
                                                      g->n_c + g->n_w + g->n_t, g->chunk_row,
                                                      g->chunk_first, g->w_ptr, g->order, g->perm,
-                                                     g->in_ptr, g->in_col, g->w_col, counters + 5);
+                                                     g->in_ptr, g->in_col, g->w_col, counters + 1,
+                                                     counters + 5);
         ++g->build_launches;
     }
     PRK_CUDA(cudaGetLastError(), "relabel launch");
 
-    // sizes for reporting: true in-edges per class, dangling count
-    const int64_t c_end = g->n_c + g->n_w + g->n_t;
-    if (c_end > 0) {
-        k_class_edges<<<grid_for(c_end, kBlock, cap), kBlock, 0, s>>>(
-            c_end, g->n_c, g->n_c + g->n_w, g->in_ptr, g->order, counters + 1);
-        ++g->build_launches;
-    }
     if (g->n_t > 0) {
         k_first_short_block<<<1, 1, 0, s>>>(g->w_ptr, g->n_c + g->n_w, (g->n_t + 31) / 32, counters + 4);
         ++g->build_launches;

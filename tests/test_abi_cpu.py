@@ -14,8 +14,12 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def header_functions():
-    with open(os.path.join(ROOT, "include", "pagerank.h")) as f:
-        text = f.read()
+    """Every function the headers under include/ declare."""
+    text = ""
+    for name in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if name.endswith(".h"):
+            with open(os.path.join(ROOT, "include", name)) as f:
+                text += f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pr_[a-z_]+)\s*\(", text)))
 
@@ -151,8 +155,20 @@ def test_run_rejects_mismatched_buffers_before_calling_the_library(monkeypatch):
         dict(out=good, x_init=np.zeros(10, dtype=np.float64)),
         dict(out=np.zeros(10, dtype=np.float32), dtype=torch.float64),
         dict(out=good, dtype=torch.int32),
+        # neither host memory nor the graph's GPU (a meta tensor stands in for
+        # another device here, where no GPU exists)
+        dict(out=torch.zeros(10, dtype=torch.float32, device="meta")),
+        dict(out=good, x_init=torch.zeros(10, dtype=torch.float32, device="meta")),
     ]
     for kw in cases:
         with pytest.raises((TypeError, ValueError)):
             g.run(0.85, 1e-6, 10, **kw)
     assert not calls
+
+
+def test_gather_rate_rejects_bad_arguments_on_host(L):
+    import ctypes
+    rate = ctypes.c_double(0.0)
+    for n, dtype, gathers, path in ((0, 0, 10, 0), (10, 2, 10, 0), (10, 0, 0, 0), (10, 0, 10, 3), (10, 0, 10, -1)):
+        st = L.pr_measure_gather_rate(n, dtype, gathers, path, ctypes.byref(rate), None)
+        assert st == prg.PR_ERR_INVALID_ARG, (n, dtype, gathers, path)

@@ -7,6 +7,9 @@ d = 0.85, tol 1e-6, at most 200 updates).
 - The converged run: iteration count within one update of the oracle's,
   |sum - 1| <= 1e-5, L1 below the tolerance, and ranks within tolerance of
   the oracle rerun for the same number of updates.
+- RMAT scale 22 also runs in its fixed-50 mode (tol = 0, exactly 50 updates,
+  the timed mode of Day 40's "Results"): every rank against the oracle after
+  the same 50 updates, and |sum - 1| <= 1e-5.
 - ER at 2^24 also runs in fp64.
 
 Each case takes tens of seconds (the oracle is single-threaded).
@@ -78,6 +81,23 @@ def test_full_size_converged(workload):
     assert_ranks_close(x, ref["x"], F32, f"{name} after {it} updates")
     refc = oracle.pagerank(rp, ci, D, tol=1e-6, max_iter=200)
     assert abs(refc["iters"] - it) <= 1, (refc["iters"], it)
+
+
+def test_rmat22_fixed_50_updates():
+    rp, ci = gg.workload("rmat22")
+    g = prg.Graph(torch.from_numpy(rp).cuda(), torch.from_numpy(ci).cuda())
+    try:
+        x, it, l1, conv = g.run(D, 0.0, 50)
+        x = x.cpu().numpy()
+    finally:
+        g.close()
+    assert it == 50 and conv   # tol <= 0: exactly max_iter updates, reported as success
+    assert abs(x.astype(np.float64).sum() - 1.0) <= F32["sum"]
+    ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=50)
+    assert ref["iters"] == 50
+    assert_ranks_close(x, ref["x"], F32, "rmat22 after 50 fixed updates")
+    # the L1 of the 50th update, against the oracle's (fp32 terms: 2% or 4 ulp(1))
+    assert abs(l1 - ref["l1"]) <= max(0.02 * ref["l1"], 4 * 2.0 ** -23), (l1, ref["l1"])
 
 
 def test_er24_fp64():

@@ -1,8 +1,10 @@
 """The random-gather rate measurement (the denominator of the update's gather
 roofline): it runs, gives a finite positive rate in a plausible range for both
-element types, and the update's own rate of gathers from L2 on a graph whose
-state does not fit in shared memory stays below what the measurement reports
-for a state of the same size (the update gathers and does more besides)."""
+element types and for every request path (the warps' loads, the TMA's
+tile::gather4 copies, both at once), and the update's own rate of gathers
+from L2 on a graph whose state does not fit in shared memory stays below what
+the measurement reports for a state of the same size (the update gathers and
+does more besides)."""
 import math
 
 import pytest
@@ -22,18 +24,20 @@ def gpu():
     build.build()
 
 
+@pytest.mark.parametrize("path", [prg.PR_GATHER_LOAD, prg.PR_GATHER_TMA, prg.PR_GATHER_BOTH])
 @pytest.mark.parametrize("dtype", [prg.PR_F32, prg.PR_F64])
 @pytest.mark.parametrize("n", [1, 1000, 1 << 22])
-def test_rate_is_finite_and_plausible(n, dtype):
-    rate = prg.pr_measure_gather_rate(n, dtype, 1 << 24)
+def test_rate_is_finite_and_plausible(n, dtype, path):
+    rate = prg.pr_measure_gather_rate(n, dtype, 1 << 24, None, path)
     assert math.isfinite(rate)
     # a random gather costs at least one cycle of an SM's L1: no GPU reaches
     # 10^13 per second, and anything below 10^9 would mean the kernel did not run
     assert 1e9 < rate < 1e13
 
 
-def test_odd_gather_count():
-    assert prg.pr_measure_gather_rate(4097, prg.PR_F32, 1001) > 0
+@pytest.mark.parametrize("path", [prg.PR_GATHER_LOAD, prg.PR_GATHER_TMA, prg.PR_GATHER_BOTH])
+def test_odd_gather_count(path):
+    assert prg.pr_measure_gather_rate(4097, prg.PR_F32, 1001, None, path) > 0
 
 
 def test_update_gathers_stay_below_the_measured_rate():
