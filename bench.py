@@ -84,6 +84,15 @@ def bytes_model(n: int, m: int) -> dict:
     return {"b_spmv": 4 * (n + 1) + 8 * m + 4 * n, "b_floor": 4 * (n + 1) + 4 * m + 8 * n}
 
 
+def build_bytes(n: int, m: int) -> int:
+    """Algorithmic bytes of the one-time transpose, as the counting sort of the
+    Day 40 page ("One iteration, three shapes of work") moves them: the
+    in-degree histogram reads col_idx (4m), the exclusive scan reads the counts
+    and writes in_ptr (8n), the scatter reads row_ptr and col_idx and writes
+    in_col (8n + 8m)."""
+    return 12 * m + 16 * n
+
+
 def day40_bytes(n: int, nnz: int) -> dict:
     """Per-iteration bytes of the Day 40 page's two implementations (4-byte
     values, 1-byte dangling mask): hand-written 8 nnz + 33 n + 4; the library
@@ -349,6 +358,16 @@ def run_ours(args, rank, world, local_rank, dist):
             "per-edge gather, y)", "peak_source": f"{peak_kind} hbm_gbs",
             "frac_of_8tbs": round(achieved / 8000.0, 4),
             "frac_floor_bytes": round(bm["b_floor"] / (per_update_ms * 1e-3) / 1e9 / peak, 4),
+        },
+        "build_roofline": {
+            "bound": "hbm", "achieved": round(build_bytes(n, m) / (transpose_ms * 1e-3) / 1e9, 1),
+            "peak": peak, "unit": "GB/s",
+            "frac": round(build_bytes(n, m) / (transpose_ms * 1e-3) / 1e9 / peak, 4),
+            "kernel": "pr_graph_create (degrees, 3 LSD radix passes by destination, in-degree scan, "
+                      "class-major work layout)",
+            "bytes_per_build": build_bytes(n, m),
+            "bytes_model": "12m + 16n (counting sort: histogram 4m, scan 8n, scatter 8m + 8n)",
+            "ms": round(transpose_ms, 4), "peak_source": f"{peak_kind} hbm_gbs",
         },
         "clocks": clocks,
         "host_wall_s": round(wall, 3), "generate_s": round(gen_s, 2),

@@ -14,13 +14,13 @@
 //      (digit, tile) its output position, and k_radix_pass ranks each tile
 //      with per-warp shared-memory counters and scatters it, staged through
 //      shared memory so that the stores are coalesced. No tile waits for
-//      another. Stable
-//      passes keep the edges into one vertex in out-edge CSR order, i.e. with
-//      ascending sources. The first pass derives each edge's source from
-//      row_ptr as it loads the edge; the last pass also produces the
-//      in-degree histogram, one atomic per run of equal destinations in a
-//      tile. A 2^24-vertex graph takes 3 passes: one counting sort over n bins
-//      would need n-entry histograms that no shared memory holds.
+//      another. Stable passes keep the edges into one vertex in out-edge CSR
+//      order, i.e. with ascending sources. The first pass's values, the
+//      edges' sources, come from k_edge_sources (row_ptr spread over the
+//      edges); the last pass also produces the in-degree histogram, one
+//      atomic per run of equal destinations in a tile. A 2^24-vertex graph
+//      takes 3 passes: one counting sort over n bins would need n-entry
+//      histograms that no shared memory holds.
 //   4. k_scan_excl   in_ptr = exclusive prefix sum of the in-degrees, in one
 //                    pass with decoupled look-back between tiles
 //
@@ -239,83 +239,6 @@ __device__ __forceinline__ int64_t tile_lo(int64_t c, int64_t tiles, int64_t cta
     return tiles * c / ctas;
 }
 
-// Upsweep of one counting-sort pass: the 256 digit counts of each CTA's tile
-// range, written digit-major (counts[d * ctas + c]), so that one exclusive
-// scan of the whole array gives every (digit, CTA) its output position. With
-// n > 0 every key is also checked against [0, n); a bad key is still
-// counted, so the downsweep's positions stay a permutation of [0, count) and
-// the build stops on the error flag before any later step reads them.
-__global__ void __launch_bounds__(kBlock)
-k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int shift,
-                int32_t *__restrict__ counts, int64_t tiles, int64_t ctas, unsigned *err)
-{
-    constexpr int kWarps = kBlock / 32;
-    __shared__ unsigned s_h[kWarps][kRadixBins];
-    const int tid = threadIdx.x, warp = tid >> 5;
-    for (int w = 0; w < kWarps; ++w)
-        s_h[w][tid] = 0;
-    __syncthreads();
-    const int64_t c = blockIdx.x;
-    const int64_t i_end = min(count, tile_lo(c + 1, tiles, ctas) * kRadixTile);
-    bool bad = false;
-    for (int64_t b = tile_lo(c, tiles, ctas) * kRadixTile; b < i_end; b += kRadixTile) {
-        int32_t v[kRadixItems];
-#pragma unroll
-        for (int k = 0; k < kRadixItems; ++k) {
-            const int64_t i = b + (int64_t)k * kBlock + tid;
-            v[k] = i < i_end ? keys[i] : 0;
-        }
-#pragma unroll
-        for (int k = 0; k < kRadixItems; ++k) {
-            if (b + (int64_t)k * kBlock + tid < i_end) {
-                bad |= n > 0 && (v[k] < 0 || (int64_t)v[k] >= n);
-                atomicAdd(&s_h[warp][((unsigned)v[k] >> shift) & (kRadixBins - 1)], 1u);
-            }
-        }
-    }
-    if (bad)
-        atomicOr(err, kErrColIdx);
-    __syncthreads();
-    unsigned t = 0;
-    for (int w = 0; w < kWarps; ++w)
-        t += s_h[w][tid];
-    counts[(int64_t)tid * ctas + c] = (int32_t)t;
-}
-
-// ---------------------------------------------------------------- step 3 --
-
-// Downsweep of one stable counting-sort pass over digit (key >> shift) & 255.
-// CTA c sorts its tile range in order. `offsets` is the exclusive scan of the
-// upsweep's digit-major counts: offsets[d * ctas + c] is where CTA c's keys of
-// digit d start, and the CTA keeps each digit's running position in shared
-// memory from tile to tile, so no CTA waits for another.
-//
-// Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
-// walks them in 32-key rounds, so "earlier round, then lower lane" is input
-// order. In each round __match_any_sync groups lanes with equal digits; a
-// per-warp shared counter carries each digit's running count across rounds.
-// Per-warp counts are then scanned across warps (and across digits for the
-// tile-local order) and the tile is staged in shared memory in (digit,
-// input) order. The write-out walks the staged tile linearly, so a warp
-// stores consecutive addresses of one bucket, and a CTA's stores of one digit
-// continue where its previous tile's ended. The next tile's keys are loaded
-// while the current one is written out.
-//
-// kFlags:
-//   kSrcRows   the values are the edges' sources: the input is the out-edge
-//              CSR's col_idx, and position i belongs to the row r with
-//              row_ptr[r] <= i < row_ptr[r+1]. The tile marks the start of
-//              every row that begins inside it and takes a max-scan, so each
-//              position learns its row without a per-key search. vals_in then
-//              holds the row of every tile's first position (k_tile_rows).
-//   kWriteKeys the keys are written too (not on the last pass).
-//   kHistogram the last pass of the edge sort: the tile, ordered by full key
-//              within each digit bucket, adds each run of equal keys to the
-//              in-degree histogram once.
-enum : unsigned { kSrcRows = 1u, kWriteKeys = 2u, kHistogram = 4u };
-
-__device__ __forceinline__ int spad(int i) { return i + (i >> 5); }   // bank-conflict padding
-
 // Block-wide inclusive max-scan of the kRadixTile entries of `a` (16-byte
 // aligned, unpadded), kRadixItems consecutive entries per thread, read and
 // written as whole int4s.
@@ -359,10 +282,125 @@ __device__ __forceinline__ void block_max_scan(int32_t *a, int32_t *s_wmax)
     __syncthreads();
 }
 
+// Upsweep of one counting-sort pass: the 256 digit counts of each CTA's tile
+// range, written digit-major (counts[d * ctas + c]), so that one exclusive
+// scan of the whole array gives every (digit, CTA) its output position. With
+// n > 0 every key is also checked against [0, n); a bad key is still
+// counted, so the downsweep's positions stay a permutation of [0, count) and
+// the build stops on the error flag before any later step reads them.
+__global__ void __launch_bounds__(kBlock)
+k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int shift,
+                int32_t *__restrict__ counts, int64_t tiles, int64_t ctas, unsigned *err)
+{
+    constexpr int kWarps = kBlock / 32;
+    __shared__ unsigned s_h[kWarps][kRadixBins];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    for (int w = 0; w < kWarps; ++w)
+        s_h[w][tid] = 0;
+    __syncthreads();
+    const int64_t c = blockIdx.x;
+    const int64_t i_end = min(count, tile_lo(c + 1, tiles, ctas) * kRadixTile);
+    bool bad = false;
+    for (int64_t b = tile_lo(c, tiles, ctas) * kRadixTile; b < i_end; b += kRadixTile) {
+        int32_t v[kRadixItems];
+#pragma unroll
+        for (int k = 0; k < kRadixItems; ++k) {
+            const int64_t i = b + (int64_t)k * kBlock + tid;
+            v[k] = i < i_end ? keys[i] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kRadixItems; ++k) {
+            if (b + (int64_t)k * kBlock + tid < i_end) {
+                bad |= n > 0 && (v[k] < 0 || (int64_t)v[k] >= n);
+                atomicAdd(&s_h[warp][((unsigned)v[k] >> shift) & (kRadixBins - 1)], 1u);
+            }
+        }
+    }
+    if (bad)
+        atomicOr(err, kErrColIdx);
+    __syncthreads();
+    unsigned t = 0;
+    for (int w = 0; w < kWarps; ++w)
+        t += s_h[w][tid];
+    counts[(int64_t)tid * ctas + c] = (int32_t)t;
+}
+
+// The source of every edge of the out-edge CSR: src[i] = the row r with
+// row_ptr[r] <= i < row_ptr[r+1], for i in [0, m), so that the first radix
+// pass reads its values like every later one. One CTA per tile of
+// kRadixTile edges (grid-stride): the rows that start inside the tile are
+// marked at their first position in shared memory and a block max-scan
+// spreads each row over its edges. tile_rows holds the row of every tile's
+// first position (k_tile_rows), so rows (tile_rows[t], tile_rows[t+1]] are
+// the only ones that can start inside tile t.
+__global__ void __launch_bounds__(kBlock)
+k_edge_sources(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ tile_rows, int64_t m,
+               int64_t tiles, int32_t *__restrict__ src)
+{
+    constexpr int kWarps = kBlock / 32;
+    __shared__ __align__(16) int32_t s_rmap[kRadixTile];
+    __shared__ int32_t s_wmax[kWarps];
+    const int tid = threadIdx.x;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t b = t * kRadixTile;
+        const int64_t rlo = tile_rows[t], rhi = tile_rows[t + 1];
+        const int tile_count = (int)min((int64_t)kRadixTile, m - b);
+        const int4 none = make_int4(INT32_MIN, INT32_MIN, INT32_MIN, INT32_MIN);
+#pragma unroll
+        for (int k = 0; k < kRadixItems / 4; ++k)
+            reinterpret_cast<int4 *>(s_rmap)[(kRadixItems / 4) * tid + k] = none;
+        __syncthreads();
+        if (tid == 0)
+            s_rmap[0] = (int32_t)rlo;
+        for (int64_t r = rlo + 1 + tid; r <= rhi; r += kBlock) {
+            const int64_t p = row_ptr[r] - b;   // rows starting past the tile are skipped
+            if (p > 0 && p < tile_count)
+                atomicMax(&s_rmap[(int)p], (int32_t)r);
+        }
+        __syncthreads();
+        block_max_scan(s_rmap, s_wmax);
+#pragma unroll
+        for (int k = 0; k < kRadixItems; ++k) {
+            const int j = k * kBlock + tid;
+            if (j < tile_count)
+                src[b + j] = s_rmap[j];
+        }
+        __syncthreads();   // the row map is read before the next tile's marks
+    }
+}
+
+// ---------------------------------------------------------------- step 3 --
+
+// Downsweep of one stable counting-sort pass over digit (key >> shift) & 255.
+// CTA c sorts its tile range in order. `offsets` is the exclusive scan of the
+// upsweep's digit-major counts: offsets[d * ctas + c] is where CTA c's keys of
+// digit d start, and the CTA keeps each digit's running position in shared
+// memory from tile to tile, so no CTA waits for another.
+//
+// Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
+// walks them in 32-key rounds, so "earlier round, then lower lane" is input
+// order. In each round __match_any_sync groups lanes with equal digits; a
+// per-warp shared counter carries each digit's running count across rounds.
+// Per-warp counts are then scanned across warps (and across digits for the
+// tile-local order) and the tile is staged in shared memory in (digit,
+// input) order. The write-out walks the staged tile linearly, so a warp
+// stores consecutive addresses of one bucket, and a CTA's stores of one digit
+// continue where its previous tile's ended. The next tile's keys are loaded
+// while the current one is written out.
+//
+// kFlags:
+//   kWriteKeys the keys are written too (not on the last pass).
+//   kHistogram the last pass of the edge sort: the tile, ordered by full key
+//              within each digit bucket, adds each run of equal keys to the
+//              in-degree histogram once.
+enum : unsigned { kWriteKeys = 2u, kHistogram = 4u };
+
+__device__ __forceinline__ int spad(int i) { return i + (i >> 5); }   // bank-conflict padding
+
 template <unsigned kFlags>
 __global__ void __launch_bounds__(kBlock, 4)
 k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ vals_in,
-             const int64_t *__restrict__ row_ptr, int64_t n, int32_t *__restrict__ keys_out,
+             int64_t n, int32_t *__restrict__ keys_out,
              int32_t *__restrict__ vals_out, int32_t *__restrict__ in_deg, int64_t count,
              int shift, const int32_t *__restrict__ offsets, int64_t tiles, int64_t ctas)
 {
@@ -375,9 +413,8 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     __shared__ unsigned s_delta[kRadixBins];        // output position - staged position, per digit
     __shared__ unsigned s_wsum[kWarps];
     __shared__ int32_t s_wmax[kWarps];
-    __shared__ __align__(16) int32_t s_key[kPadTile];   // also the row map of kSrcRows (unpadded)
+    __shared__ __align__(16) int32_t s_key[kPadTile];
     __shared__ int32_t s_val[kPadTile];
-    __shared__ int64_t s_row_lo, s_row_hi;
 
     // positions are below count <= 2^31 - 1: 32-bit indexing throughout
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -396,8 +433,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
             const int32_t i = base + r * 32 + lane;
             const bool ok = i < n_keys;
             key[r] = ok ? keys_in[i] : 0;
-            if (!(kFlags & kSrcRows))
-                val[r] = ok ? vals_in[i] : 0;
+            val[r] = ok ? vals_in[i] : 0;
         }
     };
     if (t_first < t_last)
@@ -411,36 +447,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         const int tile_count = min(kRadixTile, n_keys - tile_begin);
         const int32_t base = tile_begin + warp * kWarpSpan;
 
-        if (kFlags & kSrcRows) {
-            // row of every position of the tile: mark row starts, then max-scan.
-            // tile_rows (vals_in here) holds the row of each tile's first
-            // position, so [row of first, row of next tile's first] covers the tile.
-            int32_t *rmap = s_key;
-            if (tid == 0) {
-                s_row_lo = vals_in[tile];
-                s_row_hi = vals_in[tile + 1];
-            }
-            const int4 none = make_int4(INT32_MIN, INT32_MIN, INT32_MIN, INT32_MIN);
-#pragma unroll
-            for (int k = 0; k < kRadixItems / 4; ++k)
-                reinterpret_cast<int4 *>(rmap)[(kRadixItems / 4) * tid + k] = none;
-            __syncthreads();
-            const int64_t rlo = s_row_lo, rhi = s_row_hi;
-            if (tid == 0)
-                rmap[0] = (int32_t)rlo;
-            __syncthreads();
-            for (int64_t r = rlo + 1 + tid; r <= rhi; r += kBlock) {
-                const int64_t p = row_ptr[r] - tile_begin;   // rows starting past the tile are skipped
-                if (p > 0 && p < tile_count)
-                    atomicMax(&rmap[(int)p], (int32_t)r);
-            }
-            __syncthreads();
-            block_max_scan(rmap, s_wmax);
-#pragma unroll
-            for (int r = 0; r < kRadixItems; ++r)
-                val[r] = rmap[warp * kWarpSpan + r * 32 + lane];   // past the tile: never staged
-        }
-        __syncthreads();   // s_wh cleared; the row map read before staging reuses s_key
+        __syncthreads();   // s_wh cleared
 
         const unsigned below = (1u << lane) - 1u;
 #pragma unroll
@@ -767,9 +774,14 @@ __global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *
 // shared memory, for fp32 (kHotF32 vertices) and fp64 (kHotF64) runs: hot[0]
 // and hot[1]. All five counters are zeroed by the caller. Each thread counts
 // the entries it writes in 32 bits (a thread writes far fewer than 2^32 of
-// the m < 2^31 entries); the kernel is held to 32 registers, because the
-// perm gathers need every warp an SM can hold in flight (8 CTAs per SM).
-__global__ void __launch_bounds__(kBlock, 8)
+// the m < 2^31 entries).
+//
+// Two launches: kWide = true copies the CTA and warp classes (warps stream
+// rows; held to 32 registers, because their perm gathers need every warp an
+// SM can hold in flight, 8 CTAs per SM), kWide = false the thread class (one
+// thread per row, four perm gathers per int4 in flight; more registers).
+template <bool kWide>
+__global__ void __launch_bounds__(kBlock, kWide ? 8 : 1)
 k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t rows_end,
           const int32_t *__restrict__ chunk_row, const int32_t *__restrict__ chunk_first,
           const int32_t *__restrict__ w_ptr, const int32_t *__restrict__ order,
@@ -789,7 +801,7 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
         h64 += (w < kHotF64);
         return w;
     };
-    for (int64_t c = gwarp; c < n_chunks; c += nwarps) {
+    for (int64_t c = gwarp; kWide && c < n_chunks; c += nwarps) {
         const int32_t r = chunk_row[c];
         const int32_t v = order[r];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
@@ -801,7 +813,7 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
             w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
         }
     }
-    for (int64_t i = n_c + gwarp; i < wide_end; i += nwarps) {
+    for (int64_t i = n_c + gwarp; kWide && i < wide_end; i += nwarps) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
@@ -813,7 +825,7 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
     // thread-class rows: one thread per row, whole int4s, so the 32 lanes of
     // a warp (the 32 rows of one block) store 32 consecutive int4s
     int4 *w_col4 = reinterpret_cast<int4 *>(w_col);
-    for (int64_t i = wide_end + gtid; i < rows_end; i += nthreads) {
+    for (int64_t i = wide_end + gtid; !kWide && i < rows_end; i += nthreads) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int64_t r0 = wide_end + ((i - wide_end) & ~(int64_t)31);
@@ -959,15 +971,13 @@ int64_t sort_ctas(const pr_graph *g, int64_t tiles)
 // One counting-sort pass: upsweep (digit counts per CTA range), one
 // exclusive scan of the digit-major counts, downsweep (rank and scatter).
 template <unsigned kFlags>
-pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32_t *vin,
-                    const int64_t *row_ptr, int64_t n, int32_t *kout, int32_t *vout, int32_t *in_deg,
-                    int64_t count, int shift, int64_t validate_n, int32_t *counts, int32_t *offsets,
-                    unsigned long long *desc, unsigned *counter)
+pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32_t *vin, int64_t n,
+                    int32_t *kout, int32_t *vout, int32_t *in_deg, int64_t count, int shift, int64_t validate_n,
+                    int32_t *counts, int32_t *offsets, unsigned long long *desc, unsigned *counter)
 {
     const int64_t tiles = (count + kRadixTile - 1) / kRadixTile;
     const int64_t ctas = sort_ctas(g, tiles);
-    k_radix_upsweep<<<(unsigned)ctas, kBlock, 0, s>>>(kin, count, validate_n, shift, counts, tiles, ctas,
-                                                      g->err);
+    k_radix_upsweep<<<(unsigned)ctas, kBlock, 0, s>>>(kin, count, validate_n, shift, counts, tiles, ctas, g->err);
     ++g->build_launches;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -976,8 +986,8 @@ pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32
                                &g->build_launches, s);
     if (st != PR_OK)
         return st;
-    k_radix_pass<kFlags><<<(unsigned)ctas, kBlock, 0, s>>>(kin, vin, row_ptr, n, kout, vout, in_deg, count,
-                                                          shift, offsets, tiles, ctas);
+    k_radix_pass<kFlags><<<(unsigned)ctas, kBlock, 0, s>>>(kin, vin, n, kout, vout, in_deg, count, shift, offsets,
+                                                          tiles, ctas);
     ++g->build_launches;
     e = cudaGetLastError();
     return e == cudaSuccess ? PR_OK : cuda_status(e, "k_radix_pass launch");
@@ -1125,6 +1135,51 @@ pr_status scan_timeout_probe(int64_t count, int spin_limit, cudaStream_t s)
     return PR_OK;
 }
 
+// A second stream per device (non-blocking, created on first use, kept until
+// exit) for build work that runs beside the build's own stream. Calls from
+// several threads share it; each forks and joins with events of its own.
+static pr_status side_stream(cudaStream_t *out)
+{
+    static std::mutex mu;
+    static cudaStream_t streams[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return set_error(PR_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (streams[dev] == nullptr) {
+        e = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            streams[dev] = nullptr;
+            return cuda_status(e, "cudaStreamCreateWithFlags");
+        }
+    }
+    *out = streams[dev];
+    return PR_OK;
+}
+
+// Fork and join events of one build, destroyed when it returns (a recorded
+// event may be destroyed before it completes).
+struct EventPair {
+    cudaEvent_t fork = nullptr, join = nullptr;
+    pr_status create()
+    {
+        cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+        return e == cudaSuccess ? PR_OK : cuda_status(e, "cudaEventCreate");
+    }
+    ~EventPair()
+    {
+        if (fork)
+            cudaEventDestroy(fork);
+        if (join)
+            cudaEventDestroy(join);
+    }
+};
+
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, cudaStream_t s)
 {
     const int64_t n = g->n, m = g->m;
@@ -1221,26 +1276,34 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
                                                                             tile_rows);
         ++g->build_launches;
         PRK_CUDA(cudaGetLastError(), "k_tile_rows launch");
+        // the source of every edge, the first pass's values: a value buffer
+        // that no pass before the second writes (with two passes, in_col,
+        // which only the last pass writes)
+        int32_t *src = nullptr;
+        if (passes >= 3)
+            src = vb[1];
+        else if (passes == 2)
+            src = g->in_col;
+        else
+            PRK_TRY(tmp.alloc((void **)&src, (size_t)m * sizeof(int32_t)));
+        k_edge_sources<<<grid_for(radix_tiles, 1, g->num_sms * 8), kBlock, 0, s>>>(d_row_ptr, tile_rows, m,
+                                                                                 radix_tiles, src);
+        ++g->build_launches;
+        PRK_CUDA(cudaGetLastError(), "k_edge_sources launch");
         for (int p = 0; p < passes; ++p) {
             const int32_t *kin = p == 0 ? d_col : kb[(p - 1) & 1];
-            const int32_t *vin = p == 0 ? tile_rows : vb[(p - 1) & 1];
+            const int32_t *vin = p == 0 ? src : vb[(p - 1) & 1];
             const bool first = p == 0, last = p == passes - 1;
             int32_t *vout = last ? g->in_col : vb[p & 1];
             int32_t *kout = last ? nullptr : kb[p & 1];
             const int shift = p * kRadixBits;
             const int64_t vn = first ? n : 0;   // the first upsweep checks col_idx
-            if (first && last)
-                st = sort_pass<kSrcRows | kHistogram>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
-                                                      shift, vn, counts, offsets, desc, tile_counter);
-            else if (first)
-                st = sort_pass<kSrcRows | kWriteKeys>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m,
-                                                      shift, vn, counts, offsets, desc, tile_counter);
-            else if (last)
-                st = sort_pass<kHistogram>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m, shift, vn,
-                                           counts, offsets, desc, tile_counter);
+            if (last)
+                st = sort_pass<kHistogram>(g, s, kin, vin, n, kout, vout, in_deg, m, shift, vn, counts, offsets,
+                                           desc, tile_counter);
             else
-                st = sort_pass<kWriteKeys>(g, s, kin, vin, d_row_ptr, n, kout, vout, in_deg, m, shift, vn,
-                                           counts, offsets, desc, tile_counter);
+                st = sort_pass<kWriteKeys>(g, s, kin, vin, n, kout, vout, in_deg, m, shift, vn, counts, offsets,
+                                           desc, tile_counter);
             if (st != PR_OK)
                 return st;
             if (first) {
@@ -1266,8 +1329,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         PRK_TRY(tmp.alloc((void **)&ovals, (size_t)n * sizeof(int32_t)));
         k_order_keys<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, g->deg_out, okeys, ovals);
         ++g->build_launches;
-        PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, nullptr, n, nullptr, g->order, nullptr, n, 0, 0, counts,
-                              offsets, desc, tile_counter));
+        PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, n, nullptr, g->order, nullptr, n, 0, 0, counts, offsets, desc,
+                              tile_counter));
         k_invert<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->perm);
         ++g->build_launches;
         PRK_CUDA(cudaGetLastError(), "order launch");
@@ -1315,12 +1378,35 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
                                                                    g->chunk_row);
     PRK_CUDA(cudaGetLastError(), "chunk launch");
     if (g->m_w > 0) {
-        k_relabel<<<g->num_sms * 8, kBlock, 0, s>>>(n, g->n_c, g->n_chunks, g->n_c + g->n_w,
-                                                     g->n_c + g->n_w + g->n_t, g->chunk_row,
-                                                     g->chunk_first, g->w_ptr, g->order, g->perm,
-                                                     g->in_ptr, g->in_col, g->w_col, counters + 1,
-                                                     counters + 5);
-        ++g->build_launches;
+        // the two relabel launches run side by side: the thread-class one on
+        // a second stream, forked from and joined back to the build's stream
+        const int64_t wide_end = g->n_c + g->n_w, rows_end = wide_end + g->n_t;
+        const bool both = wide_end > 0 && g->n_t > 0;
+        cudaStream_t side = s;
+        EventPair ev;
+        if (both) {
+            PRK_TRY(side_stream(&side));
+            PRK_TRY(ev.create());
+            PRK_CUDA(cudaEventRecord(ev.fork, s), "fork");
+            PRK_CUDA(cudaStreamWaitEvent(side, ev.fork, 0), "fork");
+        }
+        if (g->n_t > 0) {
+            k_relabel<false><<<grid_for(g->n_t, kBlock, g->num_sms * 4), kBlock, 0, side>>>(
+                n, g->n_c, g->n_chunks, wide_end, rows_end, g->chunk_row, g->chunk_first, g->w_ptr, g->order,
+                g->perm, g->in_ptr, g->in_col, g->w_col, counters + 1, counters + 5);
+            ++g->build_launches;
+        }
+        if (wide_end > 0) {
+            k_relabel<true><<<g->num_sms * 8, kBlock, 0, s>>>(n, g->n_c, g->n_chunks, wide_end, rows_end,
+                                                               g->chunk_row, g->chunk_first, g->w_ptr, g->order,
+                                                               g->perm, g->in_ptr, g->in_col, g->w_col,
+                                                               counters + 1, counters + 5);
+            ++g->build_launches;
+        }
+        if (both) {
+            PRK_CUDA(cudaEventRecord(ev.join, side), "join");
+            PRK_CUDA(cudaStreamWaitEvent(s, ev.join, 0), "join");
+        }
     }
     PRK_CUDA(cudaGetLastError(), "relabel launch");
 

@@ -95,8 +95,8 @@ def test_run_rejects_bad_arguments_on_host(L, d, tol, max_iter, dtype):
                                               (1000, 0, 0), (1000, 0, (1 << 30) + 1), (1000, 7, 1024)])
 def test_gather_rate_rejects_bad_arguments_on_host(L, n, dtype, gathers):
     rate = ctypes.c_double(0.0)
-    assert L.pr_measure_gather_rate(1000, 0, 1024, None, None) == prg.PR_ERR_INVALID_ARG
-    st = L.pr_measure_gather_rate(n, dtype, gathers, ctypes.byref(rate), None)
+    assert L.pr_measure_gather_rate(1000, 0, 1024, prg.PR_GATHER_LOAD, None, None) == prg.PR_ERR_INVALID_ARG
+    st = L.pr_measure_gather_rate(n, dtype, gathers, prg.PR_GATHER_LOAD, ctypes.byref(rate), None)
     assert st == prg.PR_ERR_INVALID_ARG
     assert rate.value == 0.0
 
@@ -166,9 +166,8 @@ def test_run_rejects_mismatched_buffers_before_calling_the_library(monkeypatch):
     assert not calls
 
 
-def test_gather_rate_rejects_bad_arguments_on_host(L):
-    import ctypes
+def test_gather_rate_rejects_an_unknown_path_on_host(L):
     rate = ctypes.c_double(0.0)
-    for n, dtype, gathers, path in ((0, 0, 10, 0), (10, 2, 10, 0), (10, 0, 0, 0), (10, 0, 10, 3), (10, 0, 10, -1)):
+    for n, dtype, gathers, path in ((0, 0, 10, 1), (10, 2, 10, 2), (10, 0, 0, 1), (10, 0, 10, 3), (10, 0, 10, -1)):
         st = L.pr_measure_gather_rate(n, dtype, gathers, path, ctypes.byref(rate), None)
         assert st == prg.PR_ERR_INVALID_ARG, (n, dtype, gathers, path)
