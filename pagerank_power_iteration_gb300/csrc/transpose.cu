@@ -51,6 +51,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "pr_internal.cuh"
 
@@ -407,8 +408,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     constexpr int kWarps = kBlock / 32;
     constexpr int kWarpSpan = 32 * kRadixItems;
     constexpr int kPadTile = kRadixTile + kRadixTile / 32;
-    __shared__ unsigned s_wh[kWarps][kRadixBins];   // per-warp counts, then offsets
-    __shared__ unsigned s_start[kRadixBins];        // tile-local start of each digit
+    __shared__ unsigned s_wh[kWarps][kRadixBins];   // per-warp counts, then staged offsets
     __shared__ unsigned s_run[kRadixBins];          // next output position of each digit
     __shared__ unsigned s_delta[kRadixBins];        // output position - staged position, per digit
     __shared__ unsigned s_wsum[kWarps];
@@ -439,20 +439,21 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     if (t_first < t_last)
         load_tile(t_first);
 
-    for (int32_t tile = t_first; tile < t_last; ++tile) {
+    // One tile; kFull (every tile but the last) drops the bounds checks.
+    auto process = [&](int32_t tile, auto full) {
+        constexpr bool kFull = decltype(full)::value;
         __syncthreads();   // the previous tile's shared-memory reads are done
         for (int w = 0; w < kWarps; ++w)
             s_wh[w][tid] = 0;
         const int32_t tile_begin = tile * kRadixTile;
-        const int tile_count = min(kRadixTile, n_keys - tile_begin);
+        const int tile_count = kFull ? kRadixTile : min(kRadixTile, n_keys - tile_begin);
         const int32_t base = tile_begin + warp * kWarpSpan;
-
         __syncthreads();   // s_wh cleared
 
         const unsigned below = (1u << lane) - 1u;
 #pragma unroll
         for (int r = 0; r < kRadixItems; ++r) {
-            const bool ok = base + r * 32 + lane < n_keys;
+            const bool ok = kFull || base + r * 32 + lane < n_keys;
             const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
             const unsigned peers = __match_any_sync(0xffffffffu, dig);
             const unsigned before = ok ? s_wh[warp][dig] : 0u;
@@ -464,15 +465,13 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         }
         __syncthreads();
 
-        // thread tid owns digit tid: exclusive offsets of the warps, the
-        // tile's count, and the digit's output start for this tile
+        // thread tid owns digit tid: the tile's count of the digit, its
+        // tile-local start (exclusive scan over the 256 digits), and, per
+        // warp, where that warp's keys of the digit are staged
         unsigned tot = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            const unsigned cnt = s_wh[w][tid];
-            s_wh[w][tid] = tot;
-            tot += cnt;
-        }
-        // tile-local start of each digit (exclusive scan over the 256 digits)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            tot += s_wh[w][tid];
         const unsigned incl = warp_incl_scan(tot, lane);
         if (lane == 31)
             s_wsum[warp] = incl;
@@ -481,7 +480,13 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         for (int w = 0; w < warp; ++w)
             woff += s_wsum[w];
         const unsigned start = woff + incl - tot;
-        s_start[tid] = start;
+        unsigned run = start;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const unsigned cnt = s_wh[w][tid];
+            s_wh[w][tid] = run;
+            run += cnt;
+        }
         // staged position j of digit tid goes to s_run + (j - start); positions
         // are below count <= 2^31 - 1, so unsigned 32-bit arithmetic is exact
         s_delta[tid] = s_run[tid] - start;
@@ -491,9 +496,9 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         // stage the tile in (digit, input) order
 #pragma unroll
         for (int r = 0; r < kRadixItems; ++r) {
-            if (base + r * 32 + lane < n_keys) {
+            if (kFull || base + r * 32 + lane < n_keys) {
                 const unsigned dig = ((unsigned)key[r] >> shift) & (kRadixBins - 1);
-                const int lp = (int)(s_start[dig] + s_wh[warp][dig] + rank[r]);
+                const int lp = (int)(s_wh[warp][dig] + rank[r]);
                 s_key[spad(lp)] = key[r];
                 s_val[spad(lp)] = val[r];
             }
@@ -508,7 +513,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
 #pragma unroll
         for (int k = 0; k < kRadixItems; ++k) {
             const int i = k * kBlock + tid;
-            if (i < tile_count) {
+            if (kFull || i < tile_count) {
                 const int32_t kv = s_key[spad(i)];
                 const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
                 const unsigned pos = s_delta[dig] + (unsigned)i;
@@ -553,6 +558,12 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
                     atomicAdd(&in_deg[kv], j - head + 1);
             }
         }
+    };
+    for (int32_t tile = t_first; tile < t_last; ++tile) {
+        if (n_keys - tile * kRadixTile >= kRadixTile)
+            process(tile, std::true_type{});
+        else
+            process(tile, std::false_type{});
     }
 }
 
