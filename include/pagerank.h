@@ -110,7 +110,10 @@ typedef struct pr_run_stats {
     float loop_ms;              /* device time of the iteration loop alone (CUDA events
                                    recorded on the run's stream around the graph launch) */
     float total_ms;             /* device time from the first to the last kernel of pr_run */
-    int32_t launches;           /* kernels pr_run launched (init, one per update, output) */
+    int32_t launches;           /* kernels pr_run launched: init, the update launches
+                                   (two per trip of the graph's loop; when the loop ends
+                                   on a trip's first update, its second launch returns
+                                   at once), output */
 } pr_run_stats;
 
 /*

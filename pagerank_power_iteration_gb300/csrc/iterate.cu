@@ -401,8 +401,11 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
     const int64_t G = gridDim.x;
 
     // run scalars, read once (the last CTA rewrites them after every other
-    // CTA has passed its arrival)
+    // CTA has passed its arrival). A launch that follows the update which
+    // ended the loop, in the same trip of the WHILE body, does nothing.
     const volatile Scalars *vs = a.scal;
+    if (vs->stop)
+        return;
     const int it = vs->it;
     const double dd = vs->d, inv_n = vs->inv_n, D = vs->dmass;
     const T *__restrict__ s_old = (it & 1) ? a.s1 : a.s0;
@@ -655,9 +658,11 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         sc->it = it1;
         sc->converged = conv ? 1 : 0;
         sc->ticket = 0u;
-        __threadfence();
-        if (conv || it1 >= sc->max_iter)
+        if (conv || it1 >= sc->max_iter) {
+            sc->stop = 1;
             cudaGraphSetConditional(cond, 0);
+        }
+        __threadfence();
     }
 }
 
@@ -713,6 +718,7 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
         sc->max_iter = max_iter;
         sc->converged = 0;
         sc->ticket = 0u;
+        sc->stop = 0;
     }
 }
 
@@ -880,7 +886,13 @@ pr_status prepare_once(pr_graph *g, cudaStream_t s)
         kp.blockDim = dim3(kIterBlock);
         kp.sharedMemBytes = (unsigned)st.smem;
         kp.kernelParams = kargs;
-        e = cudaGraphAddKernelNode(&knode, cp.conditional.phGraph_out[0], nullptr, 0, &kp);
+        // the WHILE body: kUpdatesPerTrip update launches in a chain
+        cudaGraphNode_t prev = nullptr;
+        for (int k = 0; k < kUpdatesPerTrip && e == cudaSuccess; ++k) {
+            e = cudaGraphAddKernelNode(&knode, cp.conditional.phGraph_out[0], prev ? &prev : nullptr, prev ? 1 : 0,
+                                       &kp);
+            prev = knode;
+        }
     }
     if (e == cudaSuccess)
         e = cudaGraphInstantiate(&exec, graph, 0);
@@ -968,7 +980,9 @@ pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *r
     g->last.dangling_mass = hs.dmass;
     g->last.loop_ms = loop_ms;
     g->last.total_ms = total_ms;
-    g->last.launches = hs.it + 2;
+    // init, every update launch of the loop's trips (the last trip may end
+    // with launches that do nothing), output
+    g->last.launches = (hs.it + kUpdatesPerTrip - 1) / kUpdatesPerTrip * kUpdatesPerTrip + 2;
     if (iters_out)
         *iters_out = hs.it;
     if (l1_out)

@@ -35,6 +35,9 @@ constexpr int kWarpRowCost = 0;
 // classes in one order in every warp (small graphs sit in L2 and are bound
 // by fixed costs); larger ones start each warp at its own class.
 constexpr int64_t kRotateRows = (int64_t)1 << 20;
+// Update launches per trip of the CUDA graph's WHILE loop: the loop's own
+// turnaround costs more than the gap between two kernel nodes.
+constexpr int kUpdatesPerTrip = 2;
 // Work-CSR entry that pads a row to whole 16-byte loads; it gathers 0. (A
 // pad pointing at a zero slot of the state instead makes every pad of every
 // SM read one L2 line, a hot spot that was measured to cost 15 %.)
@@ -63,6 +66,9 @@ struct Scalars {
     int32_t max_iter;
     int32_t converged;
     uint32_t ticket;    // arrival counter for the last-CTA reductions
+    int32_t stop;       // 1 once an update has ended the loop (L1 < tol or the cap):
+                        // a later update launch in the same loop body does nothing
+    int32_t pad;
 };
 
 // Per-precision iteration state of a handle.

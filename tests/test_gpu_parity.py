@@ -184,10 +184,14 @@ def test_fixed_iterations(name, dtype):
     """tol <= 0 runs exactly max_iter updates (the timed fixed-50 mode)."""
     rp, ci = graph(name)
     tt = {"f32": torch.float32, "f64": torch.float64}[dtype]
-    for k in (1, 2, 50):
+    # odd and even counts: the graph's loop runs two update launches per
+    # trip, and a trip that ends on its first update must not run the second
+    for k in (1, 2, 3, 7, 50):
         with prg.Graph(rp, ci) as g:
             x, it, l1, conv = g.run(D, 0.0, k, dtype=tt)
-        assert it == k and conv
+            stats = g.last_run()
+        assert it == k and conv and stats["iterations"] == k
+        assert stats["launches"] == (k + 1) // 2 * 2 + 2   # init, the loop's launches, output
         ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=k)
         assert_ranks_close(x.cpu().numpy(), ref["x"], F32 if dtype == "f32" else F64, f"k={k}")
 
