@@ -596,20 +596,19 @@ __device__ __forceinline__ int32_t padded_degree(int32_t deg)
     return (deg + 3) & ~3;
 }
 
-// Padded length of work row i. Thread-class rows (work rows [t_begin,
-// t_end)) are stored in interleaved blocks of 32 and take the padded length
-// of their block's first row, the longest of the block (the work order sorts
-// them by length, longest first), so every row of a block has one length.
-struct LoadOrderDeg {
-    const int32_t *in_ptr;
-    const int32_t *order;
+// Padded length of work row i, from pdeg (the padded in-degrees in work
+// order). Thread-class rows (work rows [t_begin, t_end)) are stored in
+// interleaved blocks of 32 and take the padded length of their block's first
+// row, the longest of the block (the work order sorts them by length,
+// longest first), so every row of a block has one length.
+struct LoadWorkDeg {
+    const int32_t *pdeg;
     int64_t t_begin, t_end;
     __device__ int32_t operator()(int64_t i) const
     {
         if (i >= t_begin && i < t_end)
             i = t_begin + ((i - t_begin) & ~(int64_t)31);
-        const int32_t v = order[i];
-        return padded_degree(in_ptr[v + 1] - in_ptr[v]);
+        return pdeg[i];
     }
 };
 
@@ -756,13 +755,25 @@ __global__ void k_order_keys(int64_t n, const int32_t *__restrict__ in_ptr,
     }
 }
 
-__global__ void k_invert(int64_t n, const int32_t *__restrict__ order, int32_t *__restrict__ perm)
+// The inverse of the work order (perm[order[i]] = i), and, in work order, the
+// out-degrees (w_deg) and the in-degrees padded to whole int4s (pdeg, the
+// lengths the work CSR's offsets are scanned from). An entry of order outside
+// [0, n) (only if a scan before it failed) is skipped, and its row gets 0s.
+__global__ void k_invert(int64_t n, const int32_t *__restrict__ order, const int32_t *__restrict__ in_deg,
+                         const int32_t *__restrict__ deg_out, int32_t *__restrict__ perm,
+                         int32_t *__restrict__ w_deg, int32_t *__restrict__ pdeg)
 {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t v = order[i];
-        if (v >= 0 && (int64_t)v < n)
+        int32_t dout = 0, din = 0;
+        if (v >= 0 && (int64_t)v < n) {
             perm[v] = (int32_t)i;
+            dout = deg_out[v];
+            din = in_deg[v];
+        }
+        w_deg[i] = dout;
+        pdeg[i] = padded_degree(din);
     }
 }
 
@@ -892,14 +903,6 @@ __global__ void k_first_short_block(const int32_t *__restrict__ w_ptr, int64_t t
             lo = mid + 1;
     }
     *out = (unsigned long long)lo;
-}
-
-__global__ void k_permute_deg(int64_t n, const int32_t *__restrict__ order,
-                              const int32_t *__restrict__ deg_out, int32_t *__restrict__ w_deg)
-{
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x)
-        w_deg[i] = deg_out[order[i]];
 }
 
 __global__ void k_fill_chunks(int64_t n_c, int64_t n_chunks, const int32_t *__restrict__ chunk_first,
@@ -1257,21 +1260,30 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     k_outdeg<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, d_row_ptr, g->deg_out, counters, g->err);
     ++g->build_launches;
     PRK_CUDA(cudaGetLastError(), "validation launch");
-    unsigned herr = 0;
-    PRK_TRY(read_err(g, s, &herr));
-    if (herr & kErrRowPtr)
-        return set_error(PR_ERR_INVALID_GRAPH, "row_ptr is not non-decreasing");
 
-    // a look-back that gave up leaves garbage offsets: stop before they are used
-    auto check_timeout = [&]() -> pr_status {
+    // The error word is read (one stream synchronisation) right after the
+    // row_ptr check, since the row ranges of the edge-source kernel assume a
+    // non-decreasing row_ptr; after that only where the host needs a size
+    // anyway, and before any kernel that indexes an array through values an
+    // earlier step computed: a bad col_idx, or a look-back that gave up,
+    // stops the build there. Every kernel before such a check stays in
+    // bounds and ends in time whatever the values: edge sources and radix
+    // keys are only moved, radix write positions and histogram keys are
+    // range-checked, and the vertex order is inverted with a range check.
+    auto check = [&]() -> pr_status {
         unsigned w = 0;
         pr_status r = read_err(g, s, &w);
         if (r != PR_OK)
             return r;
+        if (w & kErrRowPtr)
+            return set_error(PR_ERR_INVALID_GRAPH, "row_ptr is not non-decreasing");
+        if (w & kErrColIdx)
+            return set_error(PR_ERR_INVALID_GRAPH, "col_idx has an entry outside [0, n)");
         if (w & kErrTimeout)
             return set_error(PR_ERR_TIMEOUT, "a look-back wait in the transpose gave up");
         return PR_OK;
     };
+    PRK_TRY(check());
 
     // 2 + 3: stable scatter by destination (LSD radix over 8-bit digits),
     // which also yields the in-degree histogram
@@ -1317,23 +1329,19 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
                                            desc, tile_counter);
             if (st != PR_OK)
                 return st;
-            if (first) {
-                // stop on an invalid col_idx before its destinations are used
-                PRK_TRY(read_err(g, s, &herr));
-                if (herr & kErrColIdx)
-                    return set_error(PR_ERR_INVALID_GRAPH, "col_idx has an entry outside [0, n)");
-            }
         }
     }
 
-    // 4: in_ptr = exclusive scan of the in-degrees (n + 1 outputs)
-    PRK_TRY(check_timeout());
+    // 4: in_ptr = exclusive scan of the in-degrees (n + 1 outputs), once the
+    // input is known to be valid
+    PRK_TRY(check());
     PRK_TRY(launch_scan(LoadCount{in_deg}, g->in_ptr, n, desc, tile_counter, g->err,
                         &g->build_launches, s));
-    PRK_TRY(check_timeout());
 
     // the work order: a stable counting sort of the vertices by (class,
-    // out-degree bucket), and its inverse
+    // out-degree bucket), its inverse, and the degrees in work order
+    int32_t *pdeg = nullptr;
+    PRK_TRY(tmp.alloc((void **)&pdeg, (size_t)n * sizeof(int32_t)));
     {
         int32_t *okeys = nullptr, *ovals = nullptr;
         PRK_TRY(tmp.alloc((void **)&okeys, (size_t)n * sizeof(int32_t)));
@@ -1342,7 +1350,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         ++g->build_launches;
         PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, n, nullptr, g->order, nullptr, n, 0, 0, counts, offsets, desc,
                               tile_counter));
-        k_invert<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->perm);
+        k_invert<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, in_deg, g->deg_out, g->perm, g->w_deg,
+                                                             pdeg);
         ++g->build_launches;
         PRK_CUDA(cudaGetLastError(), "order launch");
     }
@@ -1352,36 +1361,29 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     for (int q = 0; q < 4; ++q)
         PRK_CUDA(cudaMemcpyAsync(&h_cls[q], offsets + (int64_t)(q + 1) * 64 * sort_ctas(g, order_tiles), sizeof(int32_t),
                                  cudaMemcpyDeviceToHost, s), "class counts");
-    PRK_TRY(check_timeout());
+    PRK_TRY(check());
     g->n_c = h_cls[0];
     g->n_w = h_cls[1] - h_cls[0];
     g->n_t = h_cls[2] - h_cls[1];
     g->n_z = h_cls[3] - h_cls[2];
 
-    // the work CSR in class-major order
-    PRK_TRY(launch_scan(LoadOrderDeg{g->in_ptr, g->order, g->n_c + g->n_w, g->n_c + g->n_w + g->n_t},
-                        g->w_ptr, n, desc, tile_counter, g->err,
-                        &g->build_launches, s));
-    k_permute_deg<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, g->deg_out, g->w_deg);
-    ++g->build_launches;
-    int32_t h_mw = 0;
-    PRK_CUDA(cudaMemcpyAsync(&h_mw, g->w_ptr + n, sizeof(int32_t), cudaMemcpyDeviceToHost, s),
-             "work size");
-    PRK_TRY(check_timeout());
-    g->m_w = h_mw;
-    PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t), s));
-
-    // CTA rows (work rows [0, n_c)) -> chunks
+    // the work CSR's offsets in class-major order, and the chunks of the CTA
+    // rows (work rows [0, n_c)); one read of both totals
+    PRK_TRY(launch_scan(LoadWorkDeg{pdeg, g->n_c + g->n_w, g->n_c + g->n_w + g->n_t}, g->w_ptr, n, desc, tile_counter,
+                        g->err, &g->build_launches, s));
     PRK_TRY(graph_alloc(g, (void **)&g->chunk_first, (size_t)(g->n_c + 1) * sizeof(int32_t), s));
     PRK_TRY(graph_alloc(g, (void **)&g->hub_arrivals, (size_t)(g->n_c + 1) * sizeof(uint32_t), s));
     PRK_CUDA(cudaMemsetAsync(g->hub_arrivals, 0, (size_t)(g->n_c + 1) * sizeof(uint32_t), s), "memset");
     PRK_TRY(launch_scan(LoadChunkCount{g->w_ptr}, g->chunk_first, g->n_c, desc, tile_counter, g->err,
                         &g->build_launches, s));
-    int32_t h_chunks = 0;
-    PRK_CUDA(cudaMemcpyAsync(&h_chunks, g->chunk_first + g->n_c, sizeof(int32_t),
-                             cudaMemcpyDeviceToHost, s), "chunk count");
-    PRK_TRY(check_timeout());
-    g->n_chunks = h_chunks;
+    int32_t h_sizes[2] = {0, 0};   // work CSR entries, CTA-row chunks
+    PRK_CUDA(cudaMemcpyAsync(&h_sizes[0], g->w_ptr + n, sizeof(int32_t), cudaMemcpyDeviceToHost, s), "work size");
+    PRK_CUDA(cudaMemcpyAsync(&h_sizes[1], g->chunk_first + g->n_c, sizeof(int32_t), cudaMemcpyDeviceToHost, s),
+             "chunk count");
+    PRK_TRY(check());
+    g->m_w = h_sizes[0];
+    g->n_chunks = h_sizes[1];
+    PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t), s));
     PRK_TRY(graph_alloc(g, (void **)&g->chunk_row, (size_t)g->n_chunks * sizeof(int32_t), s));
     g->build_launches += (g->n_c > 0);
     if (g->n_c > 0)
@@ -1429,7 +1431,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     unsigned long long h_counters[7] = {0, 0, 0, 0, 0, 0, 0};
     PRK_CUDA(cudaMemcpyAsync(h_counters, counters, sizeof(h_counters), cudaMemcpyDeviceToHost, s),
              "counters");
-    PRK_TRY(check_timeout());
+    PRK_TRY(check());
     g->n_dangling = (int64_t)h_counters[0];
     g->e_c = (int64_t)h_counters[1];
     g->e_w = (int64_t)h_counters[2];
