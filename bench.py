@@ -61,7 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--dtype", choices=["f32", "f64"], default="f32")
     p.add_argument("--tol", type=float, default=1e-6)
     p.add_argument("--max-iter", type=int, default=200)
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-updates", type=int, default=2,
                    help="updates in the oracle's CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -122,10 +122,13 @@ def code_digest(text: str) -> str:
 
 
 def kernel_source_digest() -> str:
-    """Code digest of the update kernel's source file (and of the header it includes)."""
+    """Code digest of the update kernel's device code: iterate.cu up to its host
+    side (which starts at make_args), and the header it includes."""
     csrc = os.path.join(ROOT, "pagerank_power_iteration_gb300", "csrc")
-    text = "".join(open(os.path.join(csrc, f)).read() for f in ("iterate.cu", "pr_internal.cuh"))
-    return code_digest(text)
+    it = open(os.path.join(csrc, "iterate.cu")).read()
+    cut = it.find("IterArgs<T> make_args(pr_graph *g)")
+    device = it[:cut] if cut >= 0 else it
+    return code_digest(device + open(os.path.join(csrc, "pr_internal.cuh")).read())
 
 
 def profiled_traffic(workload: str):

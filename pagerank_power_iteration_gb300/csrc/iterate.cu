@@ -896,7 +896,13 @@ pr_status prepare_once(pr_graph *g, cudaStream_t s)
     }
     if (e == cudaSuccess)
         e = cudaGraphInstantiate(&exec, graph, 0);
+    // the graph's one-time upload to the device belongs to preparation, not
+    // to the first run's loop
+    if (e == cudaSuccess)
+        e = cudaGraphUpload(exec, s);
     if (e != cudaSuccess) {
+        if (exec)
+            cudaGraphExecDestroy(exec);
         if (graph)
             cudaGraphDestroy(graph);
         return cuda_status(e, "building the iteration graph");
