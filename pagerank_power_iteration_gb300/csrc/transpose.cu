@@ -856,14 +856,22 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
         const int64_t blk4 = w_ptr[r0] >> 2;   // rows start 16-byte aligned
         const int32_t len4 = (w_ptr[i + 1] - w_ptr[i]) >> 2;
         e_thr += (unsigned)deg;
-        for (int32_t q = 0; q < len4; ++q) {
-            const int32_t k = 4 * q;
-            int4 e;
-            e.x = (k + 0 < deg) ? relabel(in_col[src + k + 0]) : kPadSource;
-            e.y = (k + 1 < deg) ? relabel(in_col[src + k + 1]) : kPadSource;
-            e.z = (k + 2 < deg) ? relabel(in_col[src + k + 2]) : kPadSource;
-            e.w = (k + 3 < deg) ? relabel(in_col[src + k + 3]) : kPadSource;
-            w_col4[blk4 + (int64_t)q * cnt + j] = e;
+        // up to four int4s (16 entries) at a time: every load of in_col, then
+        // every perm gather, then the stores, so that a row costs two round
+        // trips to memory per 16 entries instead of two per int4
+        for (int32_t q0 = 0; q0 < len4; q0 += 4) {
+            int32_t u[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                u[k] = (4 * q0 + k < deg) ? in_col[src + 4 * q0 + k] : -1;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                u[k] = u[k] >= 0 ? relabel(u[k]) : kPadSource;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (q0 + q < len4)
+                    w_col4[blk4 + (int64_t)(q0 + q) * cnt + j] =
+                        make_int4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
         }
     }
     // per CTA: 32-bit warp sums (a warp writes far fewer than 2^32 entries),
