@@ -78,6 +78,38 @@ typedef enum pr_dtype {
     PR_F64 = 1                  /* everything in fp64 */
 } pr_dtype;
 
+/* Stages of pr_graph_create, in order (pr_graph_info.build_stage_ms). */
+#define PR_BUILD_STAGES 8
+typedef enum pr_build_stage {
+    PR_STAGE_DEGREES = 0,       /* out-degrees, dangling count, row_ptr check */
+    PR_STAGE_SOURCES = 1,       /* the source of every edge, from row_ptr */
+    PR_STAGE_SORT = 2,          /* the radix passes by destination (the stable
+                                   scatter) and the in-degree histogram */
+    PR_STAGE_OFFSETS = 3,       /* in_ptr, the exclusive scan of the in-degrees */
+    PR_STAGE_ORDER = 4,         /* the class-major vertex order and its inverse */
+    PR_STAGE_LAYOUT = 5,        /* the work CSR's offsets and the hub chunks */
+    PR_STAGE_RELABEL = 6,       /* the work CSR's sources, relabelled */
+    PR_STAGE_FINISH = 7         /* sizes for reporting */
+} pr_build_stage;
+
+/* Options of pr_graph_create_ex. A NULL pointer, or the values of
+ * PR_OPTIONS_DEFAULT, give what pr_graph_create does. */
+typedef struct pr_options {
+    int32_t thread_max;         /* rows with 1..thread_max in-edges are the thread class
+                                   (one lane per row); 1 <= thread_max <= 32. Default 32 */
+    int32_t warp_max;           /* rows with thread_max+1..warp_max in-edges are the warp
+                                   class (32-row blocks, one warp each); rows above are cut
+                                   into chunks (the "CTA" class); thread_max <= warp_max
+                                   <= 8192. Default 1024. A warp-class row's sum builds up
+                                   in one register per lane, one int4 per 32-entry step, so
+                                   the cap keeps fp32 row sums inside the parity tolerance
+                                   (a 70,000-edge row summed that way was off by 1.2e-5) */
+    int32_t stage_timing;       /* nonzero: record CUDA events between the build's stages
+                                   (pr_graph_info.build_stage_ms); default 0 */
+} pr_options;
+
+#define PR_OPTIONS_DEFAULT {32, 1024, 0}
+
 /* Sizes of the preprocessed graph (filled by pr_graph_get_info). */
 typedef struct pr_graph_info {
     int64_t n, m;
@@ -99,6 +131,12 @@ typedef struct pr_graph_info {
                                    gathers never reach L2, the other m - edges_hot
                                    gathers do */
     int64_t edges_hot_f64;      /* the same for fp64 runs (20,480 vertices) */
+    int32_t thread_max;         /* the class thresholds the handle was built with */
+    int32_t warp_max;
+    float build_ms;             /* device time of pr_graph_create's work (CUDA events on
+                                   its stream, from the first to the last launch) */
+    float build_stage_ms[PR_BUILD_STAGES];   /* device time of each stage, if the
+                                   handle was built with stage_timing; else 0 */
 } pr_graph_info;
 
 /* Statistics of the most recent pr_run on a handle (filled by pr_graph_last_run). */
@@ -135,6 +173,19 @@ typedef struct pr_run_stats {
  */
 pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
                           const int32_t *col_idx, void *stream, pr_graph **out);
+
+/*
+ * pr_graph_create with options: the in-degree class thresholds (gpu-graph-
+ * study, "PageRank T4 - degree-bucketed load balancing", uses 32 and 1024,
+ * the defaults) and per-stage timing of the build. The thresholds decide
+ * only which kernel path each row takes: the ranks agree with every
+ * setting within the rounding of the row sums. opts may be NULL. Options
+ * outside the ranges of pr_options give PR_ERR_INVALID_ARG before any work;
+ * otherwise the same arguments, results and errors as pr_graph_create.
+ */
+pr_status pr_graph_create_ex(int64_t n, int64_t m, const int64_t *row_ptr,
+                             const int32_t *col_idx, const pr_options *opts, void *stream,
+                             pr_graph **out);
 
 /*
  * Runs the power iteration on a graph.

@@ -26,6 +26,7 @@ __all__ = [
     "pr_graph_destroy", "pr_last_error", "pr_version", "pr_exclusive_scan_noalloc",
     "pr_measure_gather_rate", "PR_SCAN_NOALLOC_MAX", "PR_LAYOUT_SLACK", "max_edges", "Graph", "EXPORTED_SYMBOLS",
     "pr_test_fail_alloc_after", "pr_test_pool_used_bytes", "pr_test_scan_timeout",
+    "pr_options", "pr_graph_create_ex", "PR_BUILD_STAGES", "BUILD_STAGES",
 ]
 
 PR_OK = 0
@@ -42,13 +43,15 @@ PR_GATHER_LOAD = 0
 PR_GATHER_TMA = 1
 PR_GATHER_BOTH = 2
 
-EXPORTED_SYMBOLS = ("pr_graph_create", "pr_run", "pr_get_in_csr", "pr_graph_get_info",
+EXPORTED_SYMBOLS = ("pr_graph_create", "pr_graph_create_ex", "pr_run", "pr_get_in_csr", "pr_graph_get_info",
                     "pr_graph_last_run", "pr_graph_destroy", "pr_last_error", "pr_version",
                     "pr_exclusive_scan_noalloc", "pr_measure_gather_rate",
                     # test hooks (include/pagerank_testing.h)
                     "pr_test_fail_alloc_after", "pr_test_pool_used_bytes", "pr_test_scan_timeout")
 PR_SCAN_NOALLOC_MAX = 1 << 26
 PR_LAYOUT_SLACK = 8192
+PR_BUILD_STAGES = 8
+BUILD_STAGES = ("degrees", "sources", "sort", "offsets", "order", "layout", "relabel", "finish")
 
 
 def max_edges(n: int) -> int:
@@ -73,6 +76,11 @@ class PageRankError(RuntimeError):
         self.status = status
 
 
+class pr_options(ctypes.Structure):
+    _fields_ = [("thread_max", ctypes.c_int32), ("warp_max", ctypes.c_int32),
+                ("stage_timing", ctypes.c_int32)]
+
+
 class pr_graph_info(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("m", ctypes.c_int64), ("n_dangling", ctypes.c_int64),
                 ("rows_zero", ctypes.c_int64), ("rows_thread", ctypes.c_int64),
@@ -81,10 +89,14 @@ class pr_graph_info(ctypes.Structure):
                 ("edges_cta", ctypes.c_int64), ("cta_chunks", ctypes.c_int64),
                 ("cta_chunk_edges", ctypes.c_int32), ("iterate_grid", ctypes.c_int32),
                 ("device_bytes", ctypes.c_int64), ("build_launches", ctypes.c_int32),
-                ("edges_hot_f32", ctypes.c_int64), ("edges_hot_f64", ctypes.c_int64)]
+                ("edges_hot_f32", ctypes.c_int64), ("edges_hot_f64", ctypes.c_int64),
+                ("thread_max", ctypes.c_int32), ("warp_max", ctypes.c_int32),
+                ("build_ms", ctypes.c_float), ("build_stage_ms", ctypes.c_float * PR_BUILD_STAGES)]
 
     def as_dict(self):
-        return {k: getattr(self, k) for k, _ in self._fields_}
+        d = {k: getattr(self, k) for k, _ in self._fields_}
+        d["build_stage_ms"] = dict(zip(BUILD_STAGES, list(self.build_stage_ms)))
+        return d
 
 
 class pr_run_stats(ctypes.Structure):
@@ -114,6 +126,8 @@ def lib():
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
         L.pr_graph_create.argtypes = [i64, i64, vp, vp, vp, ctypes.POINTER(vp)]
         L.pr_graph_create.restype = ctypes.c_int
+        L.pr_graph_create_ex.argtypes = [i64, i64, vp, vp, ctypes.POINTER(pr_options), vp, ctypes.POINTER(vp)]
+        L.pr_graph_create_ex.restype = ctypes.c_int
         L.pr_run.argtypes = [vp, dbl, dbl, i32, ctypes.c_int, vp, vp,
                              ctypes.POINTER(i32), ctypes.POINTER(dbl), vp]
         L.pr_run.restype = ctypes.c_int
@@ -149,6 +163,16 @@ def pr_graph_create(n: int, m: int, row_ptr: int, col_idx: int, stream: int | No
     """Raw call: pointers as integers. Returns the handle (an integer)."""
     h = ctypes.c_void_p()
     st = lib().pr_graph_create(n, m, row_ptr, col_idx, stream, ctypes.byref(h))
+    _check(st)
+    return h.value
+
+
+def pr_graph_create_ex(n: int, m: int, row_ptr: int, col_idx: int, thread_max: int = 32,
+                       warp_max: int = 1024, stage_timing: bool = False, stream: int | None = None) -> int:
+    """Raw call with options (class thresholds, per-stage build timing). Returns the handle."""
+    opts = pr_options(int(thread_max), int(warp_max), 1 if stage_timing else 0)
+    h = ctypes.c_void_p()
+    st = lib().pr_graph_create_ex(n, m, row_ptr, col_idx, ctypes.byref(opts), stream, ctypes.byref(h))
     _check(st)
     return h.value
 
@@ -290,9 +314,12 @@ class Graph:
 
     ``row_ptr`` (int64[n+1]) and ``col_idx`` (int32[m]) form the out-edge CSR;
     they may be numpy arrays or torch tensors, on the host or on the device.
+    ``thread_max`` and ``warp_max`` are the in-degree class thresholds, and
+    ``stage_timing`` records the build's stages (``info()["build_stage_ms"]``).
     """
 
-    def __init__(self, row_ptr, col_idx, stream=None):
+    def __init__(self, row_ptr, col_idx, stream=None, thread_max: int = 32, warp_max: int = 1024,
+                 stage_timing: bool = False):
         import torch
         if isinstance(row_ptr, np.ndarray):
             row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int64)
@@ -305,8 +332,8 @@ class Graph:
         self.n = int(row_ptr.shape[0]) - 1
         self.m = int(col_idx.shape[0])
         self.device = torch.cuda.current_device()
-        self._h = pr_graph_create(self.n, self.m, _ptr(row_ptr),
-                                  _ptr(col_idx) if self.m else None, _stream(stream))
+        self._h = pr_graph_create_ex(self.n, self.m, _ptr(row_ptr), _ptr(col_idx) if self.m else None,
+                                     thread_max, warp_max, stage_timing, _stream(stream))
 
     @property
     def handle(self) -> int:

@@ -220,6 +220,20 @@ using prk::set_error;
 PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
                                  const int32_t *col_idx, void *stream, pr_graph **out)
 {
+    return pr_graph_create_ex(n, m, row_ptr, col_idx, nullptr, stream, out);
+}
+
+PR_API pr_status pr_graph_create_ex(int64_t n, int64_t m, const int64_t *row_ptr,
+                                    const int32_t *col_idx, const pr_options *opts, void *stream,
+                                    pr_graph **out)
+{
+    const pr_options o = opts ? *opts : pr_options PR_OPTIONS_DEFAULT;
+    if (o.thread_max < 1 || o.thread_max > prk::kThreadMaxLimit)
+        return set_error(PR_ERR_INVALID_ARG, "thread_max must be in [1, %d] (got %d)", prk::kThreadMaxLimit,
+                         (int)o.thread_max);
+    if (o.warp_max < o.thread_max || o.warp_max > prk::kWarpMaxLimit)
+        return set_error(PR_ERR_INVALID_ARG, "warp_max must be in [thread_max, %d] (got %d)", prk::kWarpMaxLimit,
+                         (int)o.warp_max);
     if (out == nullptr)
         return set_error(PR_ERR_INVALID_ARG, "out is NULL");
     if (n < 1)
@@ -253,6 +267,9 @@ PR_API pr_status pr_graph_create(int64_t n, int64_t m, const int64_t *row_ptr,
     g->n = n;
     g->m = m;
     g->device = dev;
+    g->thread_max = o.thread_max;
+    g->warp_max = o.warp_max;
+    g->stage_timing = o.stage_timing != 0;
     pr_status st = PR_OK;
 
     do {
@@ -399,6 +416,11 @@ PR_API pr_status pr_graph_get_info(const pr_graph *g, pr_graph_info *info)
     info->build_launches = g->build_launches;
     info->edges_hot_f32 = g->e_hot[0];
     info->edges_hot_f64 = g->e_hot[1];
+    info->thread_max = g->thread_max;
+    info->warp_max = g->warp_max;
+    info->build_ms = g->build_ms;
+    for (int k = 0; k < PR_BUILD_STAGES; ++k)
+        info->build_stage_ms[k] = g->build_stage_ms[k];
     return PR_OK;
 }
 

@@ -15,11 +15,19 @@ namespace prk {
 
 // In-degree classes of the pull SpMV (gpu-graph-study, "PageRank T4 -
 // degree-bucketed load balancing": thread per row up to 32, warp per row up
-// to 1024, block per row above). Rows above kWarpMax are cut into chunks of
-// kChunkEdges edges; each warp of the update kernel streams one contiguous
-// range of chunks, so one hub is spread over many warps and CTAs.
-constexpr int kThreadMax = 32;
-constexpr int kWarpMax = 1024;
+// to 1024, block per row above); pr_options can move both thresholds. Rows
+// above the warp threshold are cut into chunks of kChunkEdges edges; each
+// warp of the update kernel streams one contiguous range of chunks, so one
+// hub is spread over many warps and CTAs. A thread-class row is one lane's
+// work in at most eight int4s, so the thread threshold is at most 32.
+constexpr int kDefaultThreadMax = 32;
+constexpr int kDefaultWarpMax = 1024;
+constexpr int kThreadMaxLimit = 32;
+// A warp-class row is summed by one warp, each lane adding one int4 of it per
+// 32-int4 step into one register; past a few dozen steps that sequential sum
+// loses fp32 accuracy (a 70,000-edge row was off by 1.2e-5 relative), so the
+// warp threshold is capped, and longer rows go to the chunked class.
+constexpr int kWarpMaxLimit = 8192;
 constexpr int kChunkEdges = 256;
 constexpr int kBlock = 256;        // CTA size of the preprocessing kernels
 constexpr int kIterBlock = 1024;   // CTA size of the update kernel (one CTA per SM)
@@ -94,6 +102,11 @@ struct pr_graph {
     int64_t n = 0, m = 0;
     int device = 0;
     int num_sms = 0;
+    int32_t thread_max = prk::kDefaultThreadMax;   // in-degree class thresholds
+    int32_t warp_max = prk::kDefaultWarpMax;
+    bool stage_timing = false;                      // record the build's stages
+    float build_ms = 0.f;                           // device time of the build
+    float build_stage_ms[PR_BUILD_STAGES] = {};     // per stage, if recorded
 
     // in-edge CSR in the caller's vertex ids (kept for pr_get_in_csr)
     int32_t *in_ptr = nullptr;     // [n + 1]

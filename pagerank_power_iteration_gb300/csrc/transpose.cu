@@ -719,10 +719,11 @@ k_scan_excl(Load load, int32_t *__restrict__ out, int64_t count,
 // ------------------------------------------------------------ classes ---
 
 // Position of a class in the class-major order: CTA rows, warp rows, thread
-// rows, then rows without in-edges.
-__device__ __forceinline__ int class_slot(int32_t deg)
+// rows, then rows without in-edges (thresholds thread_max <= 32 <= ... as set
+// by the handle's options).
+__device__ __forceinline__ int class_slot(int32_t deg, int32_t thread_max, int32_t warp_max)
 {
-    return deg > kWarpMax ? 0 : deg > kThreadMax ? 1 : deg > 0 ? 2 : 3;
+    return deg > warp_max ? 0 : deg > thread_max ? 1 : deg > 0 ? 2 : 3;
 }
 
 // Half-octave bucket of an out-degree: 2*floor(log2(d+1)) plus the next bit.
@@ -741,13 +742,13 @@ __device__ __forceinline__ int degree_bucket(int32_t deg)
 // 32 rows one warp takes together mostly have the same length. Ties go by
 // vertex id (the sort is stable over vals = ids).
 __global__ void k_order_keys(int64_t n, const int32_t *__restrict__ in_ptr,
-                             const int32_t *__restrict__ deg_out, int32_t *__restrict__ keys,
-                             int32_t *__restrict__ vals)
+                             const int32_t *__restrict__ deg_out, int32_t thread_max, int32_t warp_max,
+                             int32_t *__restrict__ keys, int32_t *__restrict__ vals)
 {
     for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < n;
          v += (int64_t)gridDim.x * blockDim.x) {
         const int32_t indeg = in_ptr[v + 1] - in_ptr[v];
-        const int slot = class_slot(indeg);
+        const int slot = class_slot(indeg, thread_max, warp_max);
         const int ob = degree_bucket(deg_out[v]);
         const int sub = slot == 2 ? (8 - ((indeg + 3) >> 2)) * 8 + (7 - min(7, ob >> 2)) : 63 - ob;
         keys[v] = slot * 64 + sub;
@@ -1202,6 +1203,48 @@ struct EventPair {
     }
 };
 
+// CUDA events at the boundaries of the build's stages (PR_STAGE_*), on the
+// build's stream, when the handle asks for them; destroyed with the build.
+struct StageClock {
+    cudaEvent_t ev[PR_BUILD_STAGES + 1] = {};
+    bool on = false;
+    pr_status start(bool wanted, cudaStream_t s)
+    {
+        on = wanted;
+        if (!on)
+            return PR_OK;
+        for (cudaEvent_t &e : ev) {
+            const cudaError_t r = cudaEventCreate(&e);
+            if (r != cudaSuccess)
+                return cuda_status(r, "cudaEventCreate");
+        }
+        const cudaError_t r = cudaEventRecord(ev[0], s);
+        return r == cudaSuccess ? PR_OK : cuda_status(r, "cudaEventRecord");
+    }
+    // end of stage k (0-based)
+    void mark(int k, cudaStream_t s)
+    {
+        if (on)
+            cudaEventRecord(ev[k + 1], s);
+    }
+    // per-stage times once the stream has passed every mark
+    void read(float *ms) const
+    {
+        if (!on)
+            return;
+        for (int k = 0; k < PR_BUILD_STAGES; ++k)
+            if (cudaEventElapsedTime(&ms[k], ev[k], ev[k + 1]) != cudaSuccess)
+                ms[k] = 0.f;
+        cudaGetLastError();
+    }
+    ~StageClock()
+    {
+        for (cudaEvent_t e : ev)
+            if (e)
+                cudaEventDestroy(e);
+    }
+};
+
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, cudaStream_t s)
 {
     const int64_t n = g->n, m = g->m;
@@ -1209,6 +1252,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     pr_status st;
     cudaError_t e;
     Scratch tmp(s);
+    StageClock clock;
 
 #define PRK_TRY(expr)             \
     do {                          \
@@ -1222,6 +1266,10 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         if (e != cudaSuccess)                        \
             return cuda_status(e, what);             \
     } while (0)
+
+    // the build's device time (always) and its stages (when asked for)
+    PRK_CUDA(cudaEventRecord(g->ev[0], s), "cudaEventRecord");
+    PRK_TRY(clock.start(g->stage_timing, s));
 
     // handle-owned buffers: the in-edge CSR and the work layout
     PRK_TRY(graph_alloc(g, (void **)&g->in_ptr, (size_t)(n + 1) * sizeof(int32_t), s));
@@ -1292,6 +1340,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         return PR_OK;
     };
     PRK_TRY(check());
+    clock.mark(PR_STAGE_DEGREES, s);
 
     // 2 + 3: stable scatter by destination (LSD radix over 8-bit digits),
     // which also yields the in-degree histogram
@@ -1321,6 +1370,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
                                                                                  radix_tiles, src);
         ++g->build_launches;
         PRK_CUDA(cudaGetLastError(), "k_edge_sources launch");
+        clock.mark(PR_STAGE_SOURCES, s);
         for (int p = 0; p < passes; ++p) {
             const int32_t *kin = p == 0 ? d_col : kb[(p - 1) & 1];
             const int32_t *vin = p == 0 ? src : vb[(p - 1) & 1];
@@ -1340,11 +1390,16 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         }
     }
 
+    if (m == 0)
+        clock.mark(PR_STAGE_SOURCES, s);
+
     // 4: in_ptr = exclusive scan of the in-degrees (n + 1 outputs), once the
     // input is known to be valid
     PRK_TRY(check());
+    clock.mark(PR_STAGE_SORT, s);
     PRK_TRY(launch_scan(LoadCount{in_deg}, g->in_ptr, n, desc, tile_counter, g->err,
                         &g->build_launches, s));
+    clock.mark(PR_STAGE_OFFSETS, s);
 
     // the work order: a stable counting sort of the vertices by (class,
     // out-degree bucket), its inverse, and the degrees in work order
@@ -1354,7 +1409,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         int32_t *okeys = nullptr, *ovals = nullptr;
         PRK_TRY(tmp.alloc((void **)&okeys, (size_t)n * sizeof(int32_t)));
         PRK_TRY(tmp.alloc((void **)&ovals, (size_t)n * sizeof(int32_t)));
-        k_order_keys<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, g->deg_out, okeys, ovals);
+        k_order_keys<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, g->deg_out, g->thread_max,
+                                                                 g->warp_max, okeys, ovals);
         ++g->build_launches;
         PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, n, nullptr, g->order, nullptr, n, 0, 0, counts, offsets, desc,
                               tile_counter));
@@ -1370,6 +1426,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         PRK_CUDA(cudaMemcpyAsync(&h_cls[q], offsets + (int64_t)(q + 1) * 64 * sort_ctas(g, order_tiles), sizeof(int32_t),
                                  cudaMemcpyDeviceToHost, s), "class counts");
     PRK_TRY(check());
+    clock.mark(PR_STAGE_ORDER, s);
     g->n_c = h_cls[0];
     g->n_w = h_cls[1] - h_cls[0];
     g->n_t = h_cls[2] - h_cls[1];
@@ -1393,6 +1450,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     g->n_chunks = h_sizes[1];
     PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t), s));
     PRK_TRY(graph_alloc(g, (void **)&g->chunk_row, (size_t)g->n_chunks * sizeof(int32_t), s));
+    clock.mark(PR_STAGE_LAYOUT, s);
     g->build_launches += (g->n_c > 0);
     if (g->n_c > 0)
         k_fill_chunks<<<grid_for(g->n_c, 1, cap), kBlock, 0, s>>>(g->n_c, g->n_chunks, g->chunk_first,
@@ -1430,6 +1488,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         }
     }
     PRK_CUDA(cudaGetLastError(), "relabel launch");
+    clock.mark(PR_STAGE_RELABEL, s);
 
     if (g->n_t > 0) {
         k_first_short_block<<<1, 1, 0, s>>>(g->w_ptr, g->n_c + g->n_w, (g->n_t + 31) / 32, counters + 4);
@@ -1439,7 +1498,11 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     unsigned long long h_counters[7] = {0, 0, 0, 0, 0, 0, 0};
     PRK_CUDA(cudaMemcpyAsync(h_counters, counters, sizeof(h_counters), cudaMemcpyDeviceToHost, s),
              "counters");
+    clock.mark(PR_STAGE_FINISH, s);
+    PRK_CUDA(cudaEventRecord(g->ev[1], s), "cudaEventRecord");
     PRK_TRY(check());
+    cudaEventElapsedTime(&g->build_ms, g->ev[0], g->ev[1]);
+    clock.read(g->build_stage_ms);
     g->n_dangling = (int64_t)h_counters[0];
     g->e_c = (int64_t)h_counters[1];
     g->e_w = (int64_t)h_counters[2];

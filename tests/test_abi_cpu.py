@@ -171,3 +171,21 @@ def test_gather_rate_rejects_an_unknown_path_on_host(L):
     for n, dtype, gathers, path in ((0, 0, 10, 1), (10, 2, 10, 2), (10, 0, 0, 1), (10, 0, 10, 3), (10, 0, 10, -1)):
         st = L.pr_measure_gather_rate(n, dtype, gathers, path, ctypes.byref(rate), None)
         assert st == prg.PR_ERR_INVALID_ARG, (n, dtype, gathers, path)
+
+
+@pytest.mark.parametrize("thread_max,warp_max", [(0, 1024), (33, 1024), (-1, 5), (32, 31), (8, 7),
+                                                 (8, -5), (32, 8193), (1, 1 << 20)])
+def test_create_ex_rejects_bad_options_on_host(L, thread_max, warp_max):
+    opts = prg.pr_options(thread_max, warp_max, 0)
+    h = ctypes.c_void_p()
+    st = L.pr_graph_create_ex(10, 0, None, None, ctypes.byref(opts), None, ctypes.byref(h))
+    assert st == prg.PR_ERR_INVALID_ARG
+    assert ("thread_max" in prg.pr_last_error()) or ("warp_max" in prg.pr_last_error())
+    assert h.value is None
+
+
+def test_options_struct_matches_the_header():
+    hdr = open(os.path.join(ROOT, "include", "pagerank.h")).read()
+    assert "#define PR_OPTIONS_DEFAULT {32, 1024, 0}" in hdr
+    assert int(re.search(r"#define PR_BUILD_STAGES (\d+)", hdr).group(1)) == prg.PR_BUILD_STAGES
+    assert [f for f, _ in prg.pr_options._fields_] == ["thread_max", "warp_max", "stage_timing"]

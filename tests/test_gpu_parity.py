@@ -304,3 +304,45 @@ def test_invalid_graphs_are_rejected():
     with prg.Graph(rp, ci) as g:
         x, it, _, _ = g.run(D, 1e-6, 100)
     assert it > 1
+
+
+@pytest.mark.parametrize("thread_max,warp_max", [(1, 1), (8, 64), (32, 32), (16, 4096), (32, 8192)])
+@pytest.mark.parametrize("name", ["layout", "hub70k", "dups_loops", "citation30k", "rmat14"])
+def test_class_thresholds(name, thread_max, warp_max):
+    """The class thresholds move rows between kernel paths only: the transpose
+    is unchanged, the class sizes follow the thresholds, and the ranks agree
+    with the oracle at the same number of updates."""
+    rp, ci = graph(name)
+    with prg.Graph(rp, ci, thread_max=thread_max, warp_max=warp_max) as g:
+        ip, ic = g.in_csr()
+        info = g.info()
+        x, it, l1, conv = g.run(D, 1e-6, 200)
+        x = x.cpu().numpy()
+    oip, oic = oracle.transpose(rp, ci)
+    assert np.array_equal(ip.astype(np.int64), oip) and np.array_equal(ic, oic)
+    indeg = np.diff(oip)
+    assert (info["thread_max"], info["warp_max"]) == (thread_max, warp_max)
+    assert info["rows_thread"] == int(((indeg >= 1) & (indeg <= thread_max)).sum())
+    assert info["rows_warp"] == int(((indeg > thread_max) & (indeg <= warp_max)).sum())
+    assert info["rows_cta"] == int((indeg > warp_max).sum())
+    assert info["edges_cta"] == int(indeg[indeg > warp_max].sum())
+    assert info["edges_thread"] + info["edges_warp"] + info["edges_cta"] == len(ci)
+    ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=it)
+    assert_ranks_close(x, ref["x"], F32, f"{name} thresholds {thread_max}/{warp_max}")
+    refc = oracle.pagerank(rp, ci, D, tol=1e-6, max_iter=200)
+    assert abs(refc["iters"] - it) <= 1
+
+
+def test_build_stage_timing():
+    rp, ci = graph("rmat18")
+    with prg.Graph(rp, ci, stage_timing=True) as g:
+        info = g.info()
+    stages = info["build_stage_ms"]
+    assert list(stages) == list(prg.BUILD_STAGES)
+    assert all(v > 0.0 for v in stages.values()), stages
+    total = sum(stages.values())
+    # the stages tile the build from its first launch to its last
+    assert info["build_ms"] > 0.0 and abs(total - info["build_ms"]) <= 0.02 * info["build_ms"] + 0.01
+    with prg.Graph(rp, ci) as g:
+        info = g.info()
+    assert info["build_ms"] > 0.0 and all(v == 0.0 for v in info["build_stage_ms"].values())
