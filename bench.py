@@ -513,6 +513,7 @@ def run_e2e(args, rp, ci, n, m, dev, tdt, d, dist):
         g = prg.Graph(rp_h, ci_h)
         _, it, _, _ = g.run(d, args.tol, args.max_iter, dtype=tdt, out=out_h)   # synchronises
         g.close()
+        torch.cuda.synchronize(dev)   # the step ends when its frees have landed too
         step_ms.append((time.perf_counter() - ts) * 1e3)
         edges += m * it
     torch.cuda.synchronize(dev)

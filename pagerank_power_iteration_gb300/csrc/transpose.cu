@@ -1183,23 +1183,50 @@ static pr_status side_stream(cudaStream_t *out)
     return PR_OK;
 }
 
-// Fork and join events of one build, destroyed when it returns (a recorded
-// event may be destroyed before it completes).
-struct EventPair {
-    cudaEvent_t fork = nullptr, join = nullptr;
-    pr_status create()
+// Work forked from stream `main` onto stream `side` and joined back: fork()
+// makes side wait for main's work so far; the join (join(), or the
+// destructor on any early return) makes main wait for everything issued on
+// side since, so that nothing main does afterwards (freeing the build's
+// scratch, say) overtakes it. The events are destroyed with the guard (a
+// recorded event may be destroyed before it completes).
+struct ForkJoin {
+    cudaStream_t main = nullptr, side = nullptr;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+    bool forked = false;
+    pr_status fork(cudaStream_t m, cudaStream_t sd)
     {
-        cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        main = m;
+        side = sd;
+        cudaError_t e = cudaEventCreateWithFlags(&fork_ev, cudaEventDisableTiming);
         if (e == cudaSuccess)
-            e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
-        return e == cudaSuccess ? PR_OK : cuda_status(e, "cudaEventCreate");
+            e = cudaEventCreateWithFlags(&join_ev, cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(fork_ev, main);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(side, fork_ev, 0);
+        if (e != cudaSuccess)
+            return cuda_status(e, "forking the build onto a second stream");
+        forked = true;
+        return PR_OK;
     }
-    ~EventPair()
+    pr_status join()
     {
-        if (fork)
-            cudaEventDestroy(fork);
-        if (join)
-            cudaEventDestroy(join);
+        if (!forked)
+            return PR_OK;
+        forked = false;
+        cudaError_t e = cudaEventRecord(join_ev, side);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(main, join_ev, 0);
+        return e == cudaSuccess ? PR_OK : cuda_status(e, "joining the build's second stream");
+    }
+    ~ForkJoin()
+    {
+        if (forked && join() != PR_OK)
+            cudaStreamSynchronize(side);   // the join itself failed: wait outright
+        if (fork_ev)
+            cudaEventDestroy(fork_ev);
+        if (join_ev)
+            cudaEventDestroy(join_ev);
     }
 };
 
@@ -1462,12 +1489,10 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         const int64_t wide_end = g->n_c + g->n_w, rows_end = wide_end + g->n_t;
         const bool both = wide_end > 0 && g->n_t > 0;
         cudaStream_t side = s;
-        EventPair ev;
+        ForkJoin fj;
         if (both) {
             PRK_TRY(side_stream(&side));
-            PRK_TRY(ev.create());
-            PRK_CUDA(cudaEventRecord(ev.fork, s), "fork");
-            PRK_CUDA(cudaStreamWaitEvent(side, ev.fork, 0), "fork");
+            PRK_TRY(fj.fork(s, side));
         }
         if (g->n_t > 0) {
             k_relabel<false><<<grid_for(g->n_t, kBlock, g->num_sms * 4), kBlock, 0, side>>>(
@@ -1482,10 +1507,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
                                                                counters + 1, counters + 5);
             ++g->build_launches;
         }
-        if (both) {
-            PRK_CUDA(cudaEventRecord(ev.join, side), "join");
-            PRK_CUDA(cudaStreamWaitEvent(s, ev.join, 0), "join");
-        }
+        PRK_TRY(fj.join());
     }
     PRK_CUDA(cudaGetLastError(), "relabel launch");
     clock.mark(PR_STAGE_RELABEL, s);
