@@ -284,13 +284,14 @@ __device__ __forceinline__ void block_max_scan(int32_t *a, int32_t *s_wmax)
 }
 
 // Upsweep of one counting-sort pass: the 256 digit counts of each CTA's tile
-// range, written digit-major (counts[d * ctas + c]), so that one exclusive
+// range (key i at keys[i * stride]: stride 2 reads the keys of (key, value)
+// pairs), written digit-major (counts[d * ctas + c]), so that one exclusive
 // scan of the whole array gives every (digit, CTA) its output position. With
 // n > 0 every key is also checked against [0, n); a bad key is still
 // counted, so the downsweep's positions stay a permutation of [0, count) and
 // the build stops on the error flag before any later step reads them.
 __global__ void __launch_bounds__(kBlock)
-k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int shift,
+k_radix_upsweep(const int32_t *__restrict__ keys, int stride, int64_t count, int64_t n, int shift,
                 int32_t *__restrict__ counts, int64_t tiles, int64_t ctas, unsigned *err)
 {
     constexpr int kWarps = kBlock / 32;
@@ -307,7 +308,7 @@ k_radix_upsweep(const int32_t *__restrict__ keys, int64_t count, int64_t n, int 
 #pragma unroll
         for (int k = 0; k < kRadixItems; ++k) {
             const int64_t i = b + (int64_t)k * kBlock + tid;
-            v[k] = i < i_end ? keys[i] : 0;
+            v[k] = i < i_end ? keys[i * stride] : 0;
         }
 #pragma unroll
         for (int k = 0; k < kRadixItems; ++k) {
@@ -380,28 +381,36 @@ k_edge_sources(const int64_t *__restrict__ row_ptr, const int32_t *__restrict__ 
 //
 // Tile layout: warp w owns tile positions [w*32*ITEMS, (w+1)*32*ITEMS) and
 // walks them in 32-key rounds, so "earlier round, then lower lane" is input
-// order. In each round __match_any_sync groups lanes with equal digits; a
-// per-warp shared counter carries each digit's running count across rounds.
-// Per-warp counts are then scanned across warps (and across digits for the
-// tile-local order) and the tile is staged in shared memory in (digit,
-// input) order. The write-out walks the staged tile linearly, so a warp
+// order. In each round, one ballot per digit bit gives every lane the mask of
+// lanes with its digit (the native match instruction was slower, its cost
+// growing with the number of distinct digits in the warp); a per-warp shared
+// counter carries each digit's running count across rounds. Per-warp counts
+// are then scanned across warps (and across digits for the tile-local order)
+// and the tile is staged in shared memory in (digit, input) order, as (key,
+// value) pairs. The write-out walks the staged tile linearly, so a warp
 // stores consecutive addresses of one bucket, and a CTA's stores of one digit
 // continue where its previous tile's ended. The next tile's keys are loaded
 // while the current one is written out.
 //
+// Between passes each key travels with its value as one int2, so a staged
+// entry is one shared-memory store and one global store: the write-out's
+// stores scatter over a few buckets per warp, and with separate key and value
+// arrays every entry cost two such scattered stores.
+//
 // kFlags:
-//   kWriteKeys the keys are written too (not on the last pass).
+//   kPairsIn   the input is (key, value) pairs; else two arrays (first pass).
+//   kPairsOut  the output is (key, value) pairs; else the values only (last pass).
 //   kHistogram the last pass of the edge sort: the tile, ordered by full key
 //              within each digit bucket, adds each run of equal keys to the
 //              in-degree histogram once.
-enum : unsigned { kWriteKeys = 2u, kHistogram = 4u };
+enum : unsigned { kPairsIn = 1u, kPairsOut = 2u, kHistogram = 4u };
 
 __device__ __forceinline__ int spad(int i) { return i + (i >> 5); }   // bank-conflict padding
 
 template <unsigned kFlags>
 __global__ void __launch_bounds__(kBlock, 4)
 k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ vals_in,
-             int64_t n, int32_t *__restrict__ keys_out,
+             const int2 *__restrict__ pairs_in, int64_t n, int2 *__restrict__ pairs_out,
              int32_t *__restrict__ vals_out, int32_t *__restrict__ in_deg, int64_t count,
              int shift, const int32_t *__restrict__ offsets, int64_t tiles, int64_t ctas)
 {
@@ -413,8 +422,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     __shared__ unsigned s_delta[kRadixBins];        // output position - staged position, per digit
     __shared__ unsigned s_wsum[kWarps];
     __shared__ int32_t s_wmax[kWarps];
-    __shared__ __align__(16) int32_t s_key[kPadTile];
-    __shared__ int32_t s_val[kPadTile];
+    __shared__ __align__(16) int2 s_kv[kPadTile];   // staged (key, value) pairs
 
     // positions are below count <= 2^31 - 1: 32-bit indexing throughout
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -432,8 +440,14 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         for (int r = 0; r < kRadixItems; ++r) {
             const int32_t i = base + r * 32 + lane;
             const bool ok = i < n_keys;
-            key[r] = ok ? keys_in[i] : 0;
-            val[r] = ok ? vals_in[i] : 0;
+            if (kFlags & kPairsIn) {
+                const int2 kv = ok ? pairs_in[i] : make_int2(0, 0);
+                key[r] = kv.x;
+                val[r] = kv.y;
+            } else {
+                key[r] = ok ? keys_in[i] : 0;
+                val[r] = ok ? vals_in[i] : 0;
+            }
         }
     };
     if (t_first < t_last)
@@ -442,12 +456,27 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
     // One tile; kFull (every tile but the last) drops the bounds checks.
     auto process = [&](int32_t tile, auto full) {
         constexpr bool kFull = decltype(full)::value;
-        __syncthreads();   // the previous tile's shared-memory reads are done
-        for (int w = 0; w < kWarps; ++w)
-            s_wh[w][tid] = 0;
         const int32_t tile_begin = tile * kRadixTile;
         const int tile_count = kFull ? kRadixTile : min(kRadixTile, n_keys - tile_begin);
         const int32_t base = tile_begin + warp * kWarpSpan;
+        // each round's lanes with an equal digit, one ballot per digit bit;
+        // rank[] holds the masks until the ranks replace them
+#pragma unroll
+        for (int r = 0; r < kRadixItems; ++r) {
+            const bool ok = kFull || base + r * 32 + lane < n_keys;
+            const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
+            unsigned peers = 0xffffffffu;
+#pragma unroll
+            for (int b = 0; b < (kFull ? 8 : 9); ++b) {
+                const bool bit = (dig >> b) & 1u;
+                const unsigned m = __ballot_sync(0xffffffffu, bit);
+                peers &= bit ? m : ~m;
+            }
+            rank[r] = peers;
+        }
+        __syncthreads();   // the previous tile's shared-memory reads are done
+        for (int w = 0; w < kWarps; ++w)
+            s_wh[w][tid] = 0;
         __syncthreads();   // s_wh cleared
 
         const unsigned below = (1u << lane) - 1u;
@@ -455,7 +484,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         for (int r = 0; r < kRadixItems; ++r) {
             const bool ok = kFull || base + r * 32 + lane < n_keys;
             const unsigned dig = ok ? (((unsigned)key[r] >> shift) & (kRadixBins - 1)) : kRadixBins;
-            const unsigned peers = __match_any_sync(0xffffffffu, dig);
+            const unsigned peers = rank[r];
             const unsigned before = ok ? s_wh[warp][dig] : 0u;
             __syncwarp();
             rank[r] = before + __popc(peers & below);
@@ -499,8 +528,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
             if (kFull || base + r * 32 + lane < n_keys) {
                 const unsigned dig = ((unsigned)key[r] >> shift) & (kRadixBins - 1);
                 const int lp = (int)(s_wh[warp][dig] + rank[r]);
-                s_key[spad(lp)] = key[r];
-                s_val[spad(lp)] = val[r];
+                s_kv[spad(lp)] = make_int2(key[r], val[r]);
             }
         }
         __syncthreads();
@@ -514,14 +542,15 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
         for (int k = 0; k < kRadixItems; ++k) {
             const int i = k * kBlock + tid;
             if (kFull || i < tile_count) {
-                const int32_t kv = s_key[spad(i)];
-                const unsigned dig = ((unsigned)kv >> shift) & (kRadixBins - 1);
+                const int2 kv = s_kv[spad(i)];
+                const unsigned dig = ((unsigned)kv.x >> shift) & (kRadixBins - 1);
                 const unsigned pos = s_delta[dig] + (unsigned)i;
                 if (pos >= (unsigned)n_keys)   // only reachable if the offsets scan failed
                     continue;
-                vals_out[pos] = s_val[spad(i)];
-                if (kFlags & kWriteKeys)
-                    keys_out[pos] = kv;
+                if (kFlags & kPairsOut)
+                    pairs_out[pos] = kv;
+                else
+                    vals_out[pos] = kv.y;
             }
         }
 
@@ -532,7 +561,7 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
             const int j0 = tid * kRadixItems;
             int head_local = -1;
             for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j)
-                if (j == 0 || s_key[spad(j)] != s_key[spad(j - 1)])
+                if (j == 0 || s_kv[spad(j)].x != s_kv[spad(j - 1)].x)
                     head_local = j;
             int carry = head_local;
 #pragma unroll
@@ -551,10 +580,10 @@ k_radix_pass(const int32_t *__restrict__ keys_in, const int32_t *__restrict__ va
             if (lane > 0)
                 head = max(head, up);   // last run head before this thread's entries
             for (int j = j0; j < j0 + kRadixItems && j < tile_count; ++j) {
-                const int32_t kv = s_key[spad(j)];
-                if (j == 0 || kv != s_key[spad(j - 1)])
+                const int32_t kv = s_kv[spad(j)].x;
+                if (j == 0 || kv != s_kv[spad(j - 1)].x)
                     head = j;
-                if ((j == tile_count - 1 || s_key[spad(j + 1)] != kv) && kv >= 0 && (int64_t)kv < n)
+                if ((j == tile_count - 1 || s_kv[spad(j + 1)].x != kv) && kv >= 0 && (int64_t)kv < n)
                     atomicAdd(&in_deg[kv], j - head + 1);
             }
         }
@@ -994,13 +1023,16 @@ int64_t sort_ctas(const pr_graph *g, int64_t tiles)
 // One counting-sort pass: upsweep (digit counts per CTA range), one
 // exclusive scan of the digit-major counts, downsweep (rank and scatter).
 template <unsigned kFlags>
-pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32_t *vin, int64_t n,
-                    int32_t *kout, int32_t *vout, int32_t *in_deg, int64_t count, int shift, int64_t validate_n,
-                    int32_t *counts, int32_t *offsets, unsigned long long *desc, unsigned *counter)
+pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32_t *vin, const int2 *pin,
+                    int64_t n, int2 *pout, int32_t *vout, int32_t *in_deg, int64_t count, int shift,
+                    int64_t validate_n, int32_t *counts, int32_t *offsets, unsigned long long *desc,
+                    unsigned *counter)
 {
     const int64_t tiles = (count + kRadixTile - 1) / kRadixTile;
     const int64_t ctas = sort_ctas(g, tiles);
-    k_radix_upsweep<<<(unsigned)ctas, kBlock, 0, s>>>(kin, count, validate_n, shift, counts, tiles, ctas, g->err);
+    const int32_t *ukeys = (kFlags & kPairsIn) ? reinterpret_cast<const int32_t *>(pin) : kin;
+    k_radix_upsweep<<<(unsigned)ctas, kBlock, 0, s>>>(ukeys, (kFlags & kPairsIn) ? 2 : 1, count, validate_n, shift,
+                                                      counts, tiles, ctas, g->err);
     ++g->build_launches;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
@@ -1009,8 +1041,8 @@ pr_status sort_pass(pr_graph *g, cudaStream_t s, const int32_t *kin, const int32
                                &g->build_launches, s);
     if (st != PR_OK)
         return st;
-    k_radix_pass<kFlags><<<(unsigned)ctas, kBlock, 0, s>>>(kin, vin, n, kout, vout, in_deg, count, shift, offsets,
-                                                          tiles, ctas);
+    k_radix_pass<kFlags><<<(unsigned)ctas, kBlock, 0, s>>>(kin, vin, pin, n, pout, vout, in_deg, count, shift,
+                                                          offsets, tiles, ctas);
     ++g->build_launches;
     e = cudaGetLastError();
     return e == cudaSuccess ? PR_OK : cuda_status(e, "k_radix_pass launch");
@@ -1372,11 +1404,9 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     // 2 + 3: stable scatter by destination (LSD radix over 8-bit digits),
     // which also yields the in-degree histogram
     if (m > 0) {
-        int32_t *kb[2] = {nullptr, nullptr}, *vb[2] = {nullptr, nullptr};
-        for (int i = 0; i < 2 && i < passes - 1; ++i) {
-            PRK_TRY(tmp.alloc((void **)&kb[i], (size_t)m * sizeof(int32_t)));
-            PRK_TRY(tmp.alloc((void **)&vb[i], (size_t)m * sizeof(int32_t)));
-        }
+        int2 *pb[2] = {nullptr, nullptr};   // (key, value) pairs between passes
+        for (int i = 0; i < 2 && i < passes - 1; ++i)
+            PRK_TRY(tmp.alloc((void **)&pb[i], (size_t)m * sizeof(int2)));
         int32_t *tile_rows = nullptr;
         PRK_TRY(tmp.alloc((void **)&tile_rows, (size_t)(radix_tiles + 1) * sizeof(int32_t)));
         k_tile_rows<<<grid_for(radix_tiles + 1, kBlock, cap), kBlock, 0, s>>>(d_row_ptr, n, m, radix_tiles,
@@ -1388,7 +1418,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         // which only the last pass writes)
         int32_t *src = nullptr;
         if (passes >= 3)
-            src = vb[1];
+            src = reinterpret_cast<int32_t *>(pb[1]);
         else if (passes == 2)
             src = g->in_col;
         else
@@ -1399,19 +1429,23 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         PRK_CUDA(cudaGetLastError(), "k_edge_sources launch");
         clock.mark(PR_STAGE_SOURCES, s);
         for (int p = 0; p < passes; ++p) {
-            const int32_t *kin = p == 0 ? d_col : kb[(p - 1) & 1];
-            const int32_t *vin = p == 0 ? src : vb[(p - 1) & 1];
             const bool first = p == 0, last = p == passes - 1;
-            int32_t *vout = last ? g->in_col : vb[p & 1];
-            int32_t *kout = last ? nullptr : kb[p & 1];
+            const int2 *pin = first ? nullptr : pb[(p - 1) & 1];
+            int2 *pout = last ? nullptr : pb[p & 1];
             const int shift = p * kRadixBits;
             const int64_t vn = first ? n : 0;   // the first upsweep checks col_idx
-            if (last)
-                st = sort_pass<kHistogram>(g, s, kin, vin, n, kout, vout, in_deg, m, shift, vn, counts, offsets,
-                                           desc, tile_counter);
+            if (first && last)
+                st = sort_pass<kHistogram>(g, s, d_col, src, nullptr, n, nullptr, g->in_col, in_deg, m, shift, vn,
+                                           counts, offsets, desc, tile_counter);
+            else if (first)
+                st = sort_pass<kPairsOut>(g, s, d_col, src, nullptr, n, pout, nullptr, in_deg, m, shift, vn,
+                                          counts, offsets, desc, tile_counter);
+            else if (last)
+                st = sort_pass<kPairsIn | kHistogram>(g, s, nullptr, nullptr, pin, n, nullptr, g->in_col, in_deg, m,
+                                                      shift, vn, counts, offsets, desc, tile_counter);
             else
-                st = sort_pass<kWriteKeys>(g, s, kin, vin, n, kout, vout, in_deg, m, shift, vn, counts, offsets,
-                                           desc, tile_counter);
+                st = sort_pass<kPairsIn | kPairsOut>(g, s, nullptr, nullptr, pin, n, pout, nullptr, in_deg, m,
+                                                     shift, vn, counts, offsets, desc, tile_counter);
             if (st != PR_OK)
                 return st;
         }
@@ -1439,8 +1473,8 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         k_order_keys<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->in_ptr, g->deg_out, g->thread_max,
                                                                  g->warp_max, okeys, ovals);
         ++g->build_launches;
-        PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, n, nullptr, g->order, nullptr, n, 0, 0, counts, offsets, desc,
-                              tile_counter));
+        PRK_TRY(sort_pass<0u>(g, s, okeys, ovals, nullptr, n, nullptr, g->order, nullptr, n, 0, 0, counts, offsets,
+                              desc, tile_counter));
         k_invert<<<grid_for(n, kBlock, cap), kBlock, 0, s>>>(n, g->order, in_deg, g->deg_out, g->perm, g->w_deg,
                                                              pdeg);
         ++g->build_launches;
