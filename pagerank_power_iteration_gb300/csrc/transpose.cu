@@ -829,9 +829,10 @@ __global__ void k_invert(int64_t n, const int32_t *__restrict__ order, const int
 // the m < 2^31 entries).
 //
 // Two launches: kWide = true copies the CTA and warp classes (warps stream
-// rows; held to 32 registers, because their perm gathers need every warp an
-// SM can hold in flight, 8 CTAs per SM), kWide = false the thread class (one
-// thread per row, four perm gathers per int4 in flight; more registers).
+// rows, four entries per lane in flight; held to 32 registers, because their
+// perm gathers need every warp an SM can hold in flight, 8 CTAs per SM),
+// kWide = false the thread class (one thread per row, 16 perm gathers in
+// flight; more registers).
 template <bool kWide>
 __global__ void __launch_bounds__(kBlock, kWide ? 8 : 1)
 k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t rows_end,
@@ -853,26 +854,42 @@ k_relabel(int64_t n, int64_t n_c, int64_t n_chunks, int64_t wide_end, int64_t ro
         h64 += (w < kHotF64);
         return w;
     };
+    // entries [k0, k1) of one row, four loads of in_col, then four perm
+    // gathers, in flight per lane
+    auto copy = [&](int32_t src, int32_t deg, int32_t dst, int32_t k0, int32_t k1, unsigned &e) {
+        for (int32_t kb = k0; kb < k1; kb += 4 * 32) {
+            int32_t u[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int32_t k = kb + q * 32 + lane;
+                u[q] = (k < k1 && k < deg) ? in_col[src + k] : -1;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                u[q] = u[q] >= 0 ? relabel(u[q]) : kPadSource;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int32_t k = kb + q * 32 + lane;
+                if (k < k1) {
+                    e += (k < deg);
+                    w_col[dst + k] = u[q];
+                }
+            }
+        }
+    };
     for (int64_t c = gwarp; kWide && c < n_chunks; c += nwarps) {
         const int32_t r = chunk_row[c];
         const int32_t v = order[r];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int32_t dst = w_ptr[r], len = w_ptr[r + 1] - dst;
         const int32_t k0 = (int32_t)(c - chunk_first[r]) * kChunkEdges;
-        const int32_t k1 = min(k0 + kChunkEdges, len);
-        for (int32_t k = k0 + lane; k < k1; k += 32) {
-            e_cta += (k < deg);
-            w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
-        }
+        copy(src, deg, dst, k0, min(k0 + kChunkEdges, len), e_cta);
     }
     for (int64_t i = n_c + gwarp; kWide && i < wide_end; i += nwarps) {
         const int32_t v = order[i];
         const int32_t src = in_ptr[v], deg = in_ptr[v + 1] - src;
         const int32_t dst = w_ptr[i], len = w_ptr[i + 1] - dst;
-        for (int32_t k = lane; k < len; k += 32) {
-            e_warp += (k < deg);
-            w_col[dst + k] = (k < deg) ? relabel(in_col[src + k]) : kPadSource;
-        }
+        copy(src, deg, dst, 0, len, e_warp);
     }
     // thread-class rows: one thread per row, whole int4s, so the 32 lanes of
     // a warp (the 32 rows of one block) store 32 consecutive int4s
