@@ -32,7 +32,9 @@
  *    a kernel that dereferenced it would make a peer access nobody enabled.
  *  - `stream` is a cudaStream_t passed as void* (for example
  *    torch.cuda.current_stream().cuda_stream); NULL means the legacy default
- *    stream. All device work of a call is ordered on that stream.
+ *    stream. All device work of a call is ordered on that stream (work that
+ *    pr_graph_create runs on a second, library-owned stream, such as the copy
+ *    of a host col_idx, is forked from and joined back to it).
  *  - Every entry point that can fail returns a pr_status. Negative values are
  *    errors: nothing is written to the caller's output buffers and
  *    pr_last_error() returns a message (thread-local, valid until the next
@@ -134,7 +136,9 @@ typedef struct pr_graph_info {
     int32_t thread_max;         /* the class thresholds the handle was built with */
     int32_t warp_max;
     float build_ms;             /* device time of pr_graph_create's work (CUDA events on
-                                   its stream, from the first to the last launch) */
+                                   its stream, from the first to the last launch); with a
+                                   host col_idx it includes waiting for that array's copy,
+                                   which runs beside the stages that read only row_ptr */
     float build_stage_ms[PR_BUILD_STAGES];   /* device time of each stage, if the
                                    handle was built with stage_timing; else 0 */
 } pr_graph_info;

@@ -332,17 +332,15 @@ PR_API pr_status pr_graph_create_ex(int64_t n, int64_t m, const int64_t *row_ptr
                                     cudaMemcpyHostToDevice, s);
             d_rp = (const int64_t *)rp_stage;
         }
+        // a host col_idx is copied by the build itself, beside its first steps
         if (st == PR_OK && e == cudaSuccess && !ci_dev) {
             st = prk::pool_alloc(&ci_stage, (size_t)m * sizeof(int32_t), s);
-            if (st == PR_OK)
-                e = cudaMemcpyAsync(ci_stage, col_idx, (size_t)m * sizeof(int32_t),
-                                    cudaMemcpyHostToDevice, s);
             d_ci = (const int32_t *)ci_stage;
         }
         if (st == PR_OK && e != cudaSuccess)
             st = prk::cuda_status(e, "staging the input CSR");
         if (st == PR_OK)
-            st = prk::build_graph(g, d_rp, d_ci, s);
+            st = prk::build_graph(g, d_rp, d_ci, ci_dev ? nullptr : col_idx, s);
         prk::pool_free(rp_stage, s);
         prk::pool_free(ci_stage, s);
         cudaError_t se = cudaStreamSynchronize(s);

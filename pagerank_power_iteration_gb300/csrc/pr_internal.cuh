@@ -174,9 +174,13 @@ pr_status graph_alloc(pr_graph *g, void **p, size_t bytes, cudaStream_t s);
 enum PtrKind : int { kPtrHost = 0, kPtrDevice = 1, kPtrOtherDevice = 2 };
 PtrKind pointer_kind(const void *p, int device);
 
-// Transpose + classification (transpose.cu). d_row_ptr/d_col are device pointers.
+// Transpose + classification (transpose.cu). d_row_ptr/d_col are device
+// pointers. With h_col non-null, d_col is a device buffer of m entries that
+// the build fills from the host array h_col itself, on a second stream, while
+// the steps that read only row_ptr run; the copy is joined back to s before
+// the build returns, whatever it returns.
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col,
-                      cudaStream_t s);
+                      const int32_t *h_col, cudaStream_t s);
 
 // Allocation-free exclusive scan (transpose.cu).
 pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,

@@ -1321,7 +1321,8 @@ struct StageClock {
     }
 };
 
-pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, cudaStream_t s)
+pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col, const int32_t *h_col,
+                      cudaStream_t s)
 {
     const int64_t n = g->n, m = g->m;
     const int cap = g->num_sms * 32;
@@ -1346,6 +1347,20 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     // the build's device time (always) and its stages (when asked for)
     PRK_CUDA(cudaEventRecord(g->ev[0], s), "cudaEventRecord");
     PRK_TRY(clock.start(g->stage_timing, s));
+
+    // A host col_idx goes to its device buffer on the second stream while the
+    // steps that read only row_ptr (degrees, tile rows, edge sources) run on
+    // s; s waits for the copy before the first radix pass, and on any early
+    // return (the guard's destructor), so the buffer outlives the copy.
+    ForkJoin staging;
+    if (h_col != nullptr && m > 0) {
+        cudaStream_t side = s;
+        PRK_TRY(side_stream(&side));
+        PRK_TRY(staging.fork(s, side));
+        PRK_CUDA(cudaMemcpyAsync(const_cast<int32_t *>(d_col), h_col, (size_t)m * sizeof(int32_t),
+                                 cudaMemcpyHostToDevice, side),
+                 "staging col_idx");
+    }
 
     // handle-owned buffers: the in-edge CSR and the work layout
     PRK_TRY(graph_alloc(g, (void **)&g->in_ptr, (size_t)(n + 1) * sizeof(int32_t), s));
@@ -1445,6 +1460,7 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
         ++g->build_launches;
         PRK_CUDA(cudaGetLastError(), "k_edge_sources launch");
         clock.mark(PR_STAGE_SOURCES, s);
+        PRK_TRY(staging.join());   // col_idx is on the device from here on
         for (int p = 0; p < passes; ++p) {
             const bool first = p == 0, last = p == passes - 1;
             const int2 *pin = first ? nullptr : pb[(p - 1) & 1];

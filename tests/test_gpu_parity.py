@@ -111,6 +111,22 @@ def test_transpose_bit_exact(name):
     assert info["n_dangling"] == int((np.diff(rp) == 0).sum())
 
 
+def test_four_radix_passes():
+    """n > 2^24 needs a fourth 8-bit pass: the first writes (destination,
+    source) pairs, two middle passes (digits at bits 8 and 16) read and write
+    them, and the last (bits 24-31) writes the sources. Sparse, so that the
+    oracle's n-bin counting sort and updates stay quick."""
+    n = (1 << 24) + (1 << 20)
+    rp, ci = gg.random_sparse(n, 4_000_000, seed=13, dangling_frac=0.5)
+    assert (ci >= 1 << 24).sum() > 10000   # the top digit is not always 0
+    with prg.Graph(rp, ci) as g:
+        ip, ic = g.in_csr()
+    oip, oic = oracle.transpose(rp, ci)
+    assert np.array_equal(ip.astype(np.int64), oip)
+    assert np.array_equal(ic, oic)
+    _parity(rp, ci, "f32")
+
+
 def work_order(rp, ci):
     """The documented class-major work order, derived independently on the host:
     rows with in-degree > 1024, then 33..1024, then 1..32, then 0; inside the
