@@ -50,8 +50,8 @@ extern "C" {
 #endif
 
 /* Opaque handle. Owns device memory: the in-edge CSR, per-vertex out-degrees,
- * the in-degree class lists and, after the first pr_run of a precision, that
- * precision's iteration state and its instantiated CUDA graph.
+ * the in-degree class lists, the fp32 iteration state with its instantiated
+ * CUDA graph and, after the first fp64 pr_run, the same for fp64.
  *
  * Device memory (handle-owned and the build's scratch) comes from one
  * stream-ordered memory pool per device that the library creates on first
@@ -172,6 +172,10 @@ typedef struct pr_run_stats {
  *   out      receives the handle on success (untouched on failure)
  * Inputs are borrowed for the duration of the call only: the caller may free
  * or overwrite them once it returns (the call synchronises `stream`).
+ * The handle also holds the state and the iteration graph of fp32 runs
+ * (about 12 bytes per vertex, in device_bytes), built while the last build
+ * step runs on the device; those of fp64 runs are made by the first fp64
+ * pr_run.
  * Returns PR_OK, PR_ERR_INVALID_ARG, PR_ERR_INVALID_GRAPH, PR_ERR_TOO_LARGE,
  * PR_ERR_OOM, PR_ERR_TIMEOUT or PR_ERR_CUDA.
  */
@@ -206,7 +210,9 @@ pr_status pr_graph_create_ex(int64_t n, int64_t m, const int64_t *row_ptr,
  *   iters_out  optional (NULL): number of updates performed
  *   l1_out     optional (NULL): L1 distance of the last update
  * The whole loop runs on the device; the call synchronises `stream` once,
- * at the end. Returns PR_OK, PR_NOT_CONVERGED, or an error.
+ * at the end. The first PR_F64 run on a handle allocates that precision's
+ * state (PR_ERR_OOM if it cannot; the handle stays usable). Returns PR_OK,
+ * PR_NOT_CONVERGED, or an error.
  */
 pr_status pr_run(pr_graph *g, double d, double tol, int32_t max_iter,
                  pr_dtype dtype, void *ranks_out, const void *x_init,

@@ -793,7 +793,9 @@ IterArgs<T> make_args(pr_graph *g)
 }
 
 // Allocates a precision's state and builds its graph: one conditional WHILE
-// node whose body is one k_iterate launch.
+// node whose body is kUpdatesPerTrip chained k_iterate launches. Nothing here
+// reads device results on the host, so the graph is built while the device
+// still runs the work queued before it (for fp32, the end of pr_graph_create).
 template <typename T>
 pr_status prepare_once(pr_graph *g, cudaStream_t s);
 
@@ -826,8 +828,11 @@ pr_status prepare_once(pr_graph *g, cudaStream_t s)
     const int64_t hot_cap = kHotBytes / (int64_t)sizeof(T);
     st.hot = (int32_t)(g->n + 1 < hot_cap ? g->n + 1 : hot_cap);
     st.smem = (size_t)st.hot * sizeof(T);
-    cudaError_t e = cudaFuncSetAttribute(k_iterate<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)st.smem);
+    // the kernel's limit is set to the largest copy any handle asks for, not
+    // to this handle's: handles prepared from several host threads at once
+    // then all write the same value, and no handle's graph is instantiated
+    // while another thread has lowered the limit below its own size
+    cudaError_t e = cudaFuncSetAttribute(k_iterate<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kHotBytes);
     if (e != cudaSuccess)
         return cuda_status(e, "shared memory attribute");
     int per_sm = 0;
@@ -855,8 +860,6 @@ pr_status prepare_once(pr_graph *g, cudaStream_t s)
     const int sg = (int)((warps + 1 + kBlock - 1) / kBlock);
     k_split<<<sg, kBlock, 0, s>>>(g->w_ptr, w0, w1, warps, kWarpRowCost, st.w_split);
     e = cudaGetLastError();
-    if (e == cudaSuccess)
-        e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_status(e, "splitting the classes");
 
@@ -999,6 +1002,11 @@ pr_status run_typed(pr_graph *g, double d, double tol, int32_t max_iter, void *r
 }
 
 }  // namespace
+
+pr_status prepare_dtype(pr_graph *g, int dtype, cudaStream_t s)
+{
+    return dtype == PR_F64 ? prepare<double>(g, s) : prepare<float>(g, s);
+}
 
 pr_status run(pr_graph *g, double d, double tol, int32_t max_iter, int dtype, void *ranks_out,
               const void *x_init, int32_t *iters_out, double *l1_out, cudaStream_t s)

@@ -182,6 +182,10 @@ PtrKind pointer_kind(const void *p, int device);
 pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_col,
                       const int32_t *h_col, cudaStream_t s);
 
+// A precision's state and iteration graph (iterate.cu), built once per handle:
+// by pr_graph_create for fp32, by the first pr_run of fp64.
+pr_status prepare_dtype(pr_graph *g, int dtype, cudaStream_t s);
+
 // Allocation-free exclusive scan (transpose.cu).
 pr_status exclusive_scan_noalloc(const int32_t *counts, int32_t *offsets, int64_t count,
                                  cudaStream_t s);

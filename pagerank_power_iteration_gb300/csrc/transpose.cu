@@ -1535,13 +1535,21 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     PRK_CUDA(cudaMemsetAsync(g->hub_arrivals, 0, (size_t)(g->n_c + 1) * sizeof(uint32_t), s), "memset");
     PRK_TRY(launch_scan(LoadChunkCount{g->w_ptr}, g->chunk_first, g->n_c, desc, tile_counter, g->err,
                         &g->build_launches, s));
+    if (g->n_t > 0) {
+        k_first_short_block<<<1, 1, 0, s>>>(g->w_ptr, g->n_c + g->n_w, (g->n_t + 31) / 32, counters + 4);
+        ++g->build_launches;
+    }
+    PRK_CUDA(cudaGetLastError(), "short-block launch");
     int32_t h_sizes[2] = {0, 0};   // work CSR entries, CTA-row chunks
+    unsigned long long h_short = 0;
     PRK_CUDA(cudaMemcpyAsync(&h_sizes[0], g->w_ptr + n, sizeof(int32_t), cudaMemcpyDeviceToHost, s), "work size");
     PRK_CUDA(cudaMemcpyAsync(&h_sizes[1], g->chunk_first + g->n_c, sizeof(int32_t), cudaMemcpyDeviceToHost, s),
              "chunk count");
+    PRK_CUDA(cudaMemcpyAsync(&h_short, counters + 4, sizeof(h_short), cudaMemcpyDeviceToHost, s), "short blocks");
     PRK_TRY(check());
     g->m_w = h_sizes[0];
     g->n_chunks = h_sizes[1];
+    g->t_short = (int64_t)h_short;
     PRK_TRY(graph_alloc(g, (void **)&g->w_col, (size_t)(g->m_w + 4) * sizeof(int32_t), s));
     PRK_TRY(graph_alloc(g, (void **)&g->chunk_row, (size_t)g->n_chunks * sizeof(int32_t), s));
     clock.mark(PR_STAGE_LAYOUT, s);
@@ -1579,11 +1587,10 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     PRK_CUDA(cudaGetLastError(), "relabel launch");
     clock.mark(PR_STAGE_RELABEL, s);
 
-    if (g->n_t > 0) {
-        k_first_short_block<<<1, 1, 0, s>>>(g->w_ptr, g->n_c + g->n_w, (g->n_t + 31) / 32, counters + 4);
-        ++g->build_launches;
-    }
-    PRK_CUDA(cudaGetLastError(), "short-block launch");
+    // the fp32 run's state and iteration graph, built on the host while the
+    // relabel runs (pr_run would otherwise build them with the device idle)
+    PRK_TRY(prepare_dtype(g, PR_F32, s));
+
     unsigned long long h_counters[7] = {0, 0, 0, 0, 0, 0, 0};
     PRK_CUDA(cudaMemcpyAsync(h_counters, counters, sizeof(h_counters), cudaMemcpyDeviceToHost, s),
              "counters");
@@ -1596,7 +1603,6 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     g->e_c = (int64_t)h_counters[1];
     g->e_w = (int64_t)h_counters[2];
     g->e_t = (int64_t)h_counters[3];
-    g->t_short = (int64_t)h_counters[4];
     g->e_hot[0] = (int64_t)h_counters[5];
     g->e_hot[1] = (int64_t)h_counters[6];
     return PR_OK;

@@ -1,8 +1,8 @@
 """Failure paths of the library, exercised without faulting a GPU.
 
 - PR_ERR_OOM: the test hook makes the k-th allocation from the library's
-  pool fail on the host, for every k that pr_graph_create (and the first
-  pr_run of a precision) reaches. Each failure must return PR_ERR_OOM, hand
+  pool fail on the host, for every k that pr_graph_create (which also makes
+  the fp32 run state) and the first fp64 pr_run reach. Each failure must return PR_ERR_OOM, hand
   every block back to the pool (the pool's used bytes return to where they
   were), and leave the library usable: the next call succeeds and gives the
   same result as a run that never failed.
@@ -72,16 +72,25 @@ def test_injected_allocation_failures_in_create_leak_nothing():
 
 
 def test_injected_allocation_failures_in_run_leak_nothing():
+    # the fp32 state is made by pr_graph_create, the fp64 state by the first
+    # fp64 run: that run is the one that allocates
     rp, ci = gg.citation(n=5000, seed=3)
-    ref, _ = reference_ranks(rp, ci)
+    with prg.Graph(rp, ci) as g:
+        ref = g.run(0.85, 0.0, 5, dtype=torch.float64)[0].cpu().numpy()
     with prg.Graph(rp, ci) as g:
         base = prg.pr_test_pool_used_bytes()
         info0 = g.info()
+        prg.pr_test_fail_alloc_after(1)
+        try:
+            g.run(0.85, 0.0, 5)   # fp32: allocates nothing, so the hook does not fire
+        finally:
+            prg.pr_test_fail_alloc_after(0)
+        assert prg.pr_test_pool_used_bytes() == base
         failures = 0
         for k in range(1, 50):
             prg.pr_test_fail_alloc_after(k)
             try:
-                x, it, _, _ = g.run(0.85, 0.0, 5)
+                x, it, _, _ = g.run(0.85, 0.0, 5, dtype=torch.float64)
             except prg.PageRankError as e:
                 assert e.status == prg.PR_ERR_OOM, str(e)
                 assert prg.pr_test_pool_used_bytes() == base, f"allocation {k}: memory leaked"
