@@ -322,6 +322,30 @@ def test_invalid_graphs_are_rejected():
     assert it > 1
 
 
+def test_bad_row_ptr_while_host_col_idx_is_copied():
+    """A host col_idx is copied on the library's second stream while the
+    row_ptr-only steps run; a bad row_ptr stops the build there, with the copy
+    (1.2 ms for RMAT-22's 261 MB) still in flight. The build must wait for it
+    before its buffer goes back to the pool, and the next build from host
+    arrays must equal one from device arrays."""
+    rp, ci = gg.workload("rmat22")
+    rbad = rp.copy()
+    k = len(rbad) // 2
+    rbad[k] = rbad[k + 1] + 1   # row_ptr decreases once; row_ptr[n] = m still
+    for _ in range(3):
+        with pytest.raises(prg.PageRankError) as e:
+            prg.Graph(rbad, ci)
+        assert e.value.status == prg.PR_ERR_INVALID_GRAPH
+    with prg.Graph(rp, ci) as g:
+        ip, ic = g.in_csr()
+        x, it, _, _ = g.run(D, 1e-6, 200)
+    with prg.Graph(torch.from_numpy(rp).cuda(), torch.from_numpy(ci).cuda()) as g:
+        ip2, ic2 = g.in_csr()
+        x2, it2, _, _ = g.run(D, 1e-6, 200)
+    assert np.array_equal(ip, ip2) and np.array_equal(ic, ic2)
+    assert it == it2 and torch.equal(x, x2)
+
+
 @pytest.mark.parametrize("thread_max,warp_max", [(1, 1), (8, 64), (32, 32), (16, 4096), (32, 8192)])
 @pytest.mark.parametrize("name", ["layout", "hub70k", "dups_loops", "citation30k", "rmat14"])
 def test_class_thresholds(name, thread_max, warp_max):
