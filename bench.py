@@ -526,6 +526,7 @@ def run_e2e(args, rp, ci, n, m, dev, tdt, d, dist):
     return {"value": round(edges / dt / 1e9, 3), "unit": UNIT,
             "h2d_bytes_per_step": 8 * (n + 1) + 4 * m, "d2h_bytes_per_step": elt * n,
             "steps": k, "ms_per_step": round(dt / k * 1e3, 3),
+            "ms_per_step_median": round(sorted(step_ms)[len(step_ms) // 2], 3),
             "step_ms_min_max": [round(min(step_ms), 3), round(max(step_ms), 3)],
             "step_ms": [round(x, 3) for x in step_ms],
             "create_ms": [round(x, 3) for x in create_ms],   # of step_ms: Graph() from host memory
