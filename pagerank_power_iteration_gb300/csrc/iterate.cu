@@ -20,7 +20,9 @@
 //     row sums with a segmented scan; rows of 1..32 in-edges one per lane,
 //     sorted by length and stored interleaved by blocks of 32, each warp
 //     reading where its next 32 blocks lie before it starts them; rows
-//     without in-edges take the constant term only. Every row is padded to
+//     without in-edges take the constant term only (after the first update,
+//     those that have no out-edges either are not touched: they all add the
+//     same L1 and dangling terms, counted once). Every row is padded to
 //     whole 16-byte index loads. Each warp takes the three gathering classes
 //     in its own order (starting at class warp % 3), so the classes run side
 //     by side on every SM;
@@ -64,6 +66,7 @@ struct IterArgs {
     const int32_t *deg_out;   // out-degrees by vertex id
     const int32_t *w_split;   // [warps + 1]: warp-class rows of each warp of the grid
     int64_t n, n_c, n_w, n_t, n_z, n_chunks;
+    int64_t n_iso;            // the last rows of the zero class: no in- and no out-edges
     int64_t t_short;          // first thread-class block whose rows span at most two int4s
     int rotate;               // 1: warp w starts at gather class w % 3
 };
@@ -432,22 +435,33 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
             s_hot[u] = s_old[u];
     }
 
-    // rows without in-edges: x' = base; eight rows per thread in flight
+    // rows without in-edges: x' = base; eight rows per thread in flight.
+    // From the second update on, the isolated rows at the end of the class
+    // (no out-edges either, so never gathered) are not touched: each had
+    // x = the previous update's base, so together they add n_iso times one
+    // L1 term and one dangling term, and the output takes their rank from
+    // base_last. The integer sums are the same as row by row.
     {
         const int64_t z0 = a.n - a.n_z, stride = G * kIterBlock;
-        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < a.n; i += 8 * stride) {
+        const int64_t z_end = it == 0 ? a.n : a.n - a.n_iso;
+        for (int64_t i = z0 + (int64_t)blockIdx.x * kIterBlock + tid; i < z_end; i += 8 * stride) {
             int32_t dg[8];
             T so[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t)
-                if (i + t * stride < a.n) {
+                if (i + t * stride < z_end) {
                     dg[t] = a.w_deg[i + t * stride];
                     so[t] = s_old[i + t * stride];
                 }
 #pragma unroll
             for (int t = 0; t < 8; ++t)
-                if (i + t * stride < a.n)
+                if (i + t * stride < z_end)
                     combine_row(i + t * stride, T(0), dg[t], so[t], s_new, base, d, l1, dm);
+        }
+        if (it > 0 && a.n_iso > 0 && blockIdx.x == 0 && tid == 0) {
+            const T prev = T(vs->base_last);
+            l1 += (unsigned long long)a.n_iso * to_fixed(abs_t(base - prev));
+            dm += (unsigned long long)a.n_iso * to_fixed(base);
         }
     }
     cp_async_wait_all();
@@ -658,6 +672,7 @@ k_iterate(IterArgs<T> a, int32_t hot, cudaGraphConditionalHandle cond)
         sc->it = it1;
         sc->converged = conv ? 1 : 0;
         sc->ticket = 0u;
+        sc->base_last = (double)base;
         if (conv || it1 >= sc->max_iter) {
             sc->stop = 1;
             cudaGraphSetConditional(cond, 0);
@@ -719,6 +734,7 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
         sc->converged = 0;
         sc->ticket = 0u;
         sc->stop = 0;
+        sc->base_last = 0.0;
     }
 }
 
@@ -727,12 +743,16 @@ k_init(IterArgs<T> a, const T *__restrict__ x_init, double d, double tol, int32_
 template <typename T>
 __global__ void k_output(IterArgs<T> a, T *__restrict__ out)
 {
-    const int it = ((const volatile Scalars *)a.scal)->it;
+    const volatile Scalars *vs = a.scal;
+    const int it = vs->it;
+    const T base_last = T(vs->base_last);
+    const int64_t iso0 = a.n - a.n_iso;   // isolated rows keep no state after the first update
     const T *s = (it & 1) ? a.s1 : a.s0;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < a.n;
          v += (int64_t)gridDim.x * blockDim.x) {
         const int32_t deg = a.deg_out[v];
-        const T sv = s[a.perm[v]];
+        const int32_t p = a.perm[v];
+        const T sv = p >= iso0 ? base_last : s[p];
         out[v] = deg ? sv * T(deg) : sv;
     }
 }
@@ -787,6 +807,7 @@ IterArgs<T> make_args(pr_graph *g)
     a.n_t = g->n_t;
     a.n_z = g->n_z;
     a.n_chunks = g->n_chunks;
+    a.n_iso = g->n_iso;
     a.t_short = g->t_short;
     a.rotate = (g->n - g->n_z >= kRotateRows) ? 1 : 0;
     return a;

@@ -70,6 +70,8 @@ struct Scalars {
     double d;           // damping factor
     double tol;         // L1 tolerance (<= 0: fixed number of updates)
     double inv_n;       // 1/n
+    double base_last;   // the constant term (1-d)/n + d D/n of the last update, in the
+                        // run's precision: the rank of every vertex without in-edges
     int32_t it;         // updates performed so far
     int32_t max_iter;
     int32_t converged;
@@ -128,6 +130,8 @@ struct pr_graph {
     int32_t *chunk_first = nullptr;  // [n_c + 1]: first chunk of each CTA row
     uint32_t *hub_arrivals = nullptr; // [n_c]: chunks of the row finished this update
     int64_t n_dangling = 0, n_z = 0, n_t = 0, n_w = 0, n_c = 0, n_chunks = 0;
+    // the last n_iso work rows: vertices with neither in- nor out-edges
+    int64_t n_iso = 0;
     // thread-class rows come in blocks of 32 sorted by length, longest first;
     // blocks [t_short, ...) have rows of at most two int4s
     int64_t t_short = 0;

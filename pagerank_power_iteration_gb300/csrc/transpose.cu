@@ -1515,16 +1515,21 @@ pr_status build_graph(pr_graph *g, const int64_t *d_row_ptr, const int32_t *d_co
     }
     // class sizes: the scanned counts at the digit boundaries 64, 128, 192, 256
     // (keys are class * 64 + bucket)
-    int32_t h_cls[4];
+    int32_t h_cls[5];
     for (int q = 0; q < 4; ++q)
         PRK_CUDA(cudaMemcpyAsync(&h_cls[q], offsets + (int64_t)(q + 1) * 64 * sort_ctas(g, order_tiles), sizeof(int32_t),
                                  cudaMemcpyDeviceToHost, s), "class counts");
+    // key 255 (no in-edges, out-degree bucket of 0) holds exactly the vertices
+    // with neither in- nor out-edges: the tail of the order
+    PRK_CUDA(cudaMemcpyAsync(&h_cls[4], offsets + (int64_t)255 * sort_ctas(g, order_tiles), sizeof(int32_t),
+                             cudaMemcpyDeviceToHost, s), "isolated count");
     PRK_TRY(check());
     clock.mark(PR_STAGE_ORDER, s);
     g->n_c = h_cls[0];
     g->n_w = h_cls[1] - h_cls[0];
     g->n_t = h_cls[2] - h_cls[1];
     g->n_z = h_cls[3] - h_cls[2];
+    g->n_iso = h_cls[3] - h_cls[4];
 
     // the work CSR's offsets in class-major order, and the chunks of the CTA
     // rows (work rows [0, n_c)); one read of both totals
