@@ -256,7 +256,7 @@ pr_status pr_graph_last_run(const pr_graph *g, pr_run_stats *stats);
  *   count    0 <= count <= PR_SCAN_NOALLOC_MAX; larger counts are rejected
  *            with PR_ERR_TOO_LARGE and a message
  * Scratch: the look-back descriptors live in one fixed file-scope device
- * array sized for PR_SCAN_NOALLOC_MAX elements (about 128 KB), which every
+ * array sized for PR_SCAN_NOALLOC_MAX elements (about 64 KB), which every
  * device that loads the library holds until the process exits. The first
  * call on a device looks up that array's device address
  * (cudaGetSymbolAddress) with the device current; make that first call

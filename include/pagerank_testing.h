@@ -48,7 +48,8 @@ pr_status pr_test_pool_used_bytes(int64_t *used);
  * the error word and finishes. Every CTA reads and writes only inside the
  * call's own buffers. Returns PR_ERR_TIMEOUT when a wait ran out (the
  * expected outcome), PR_OK if none did, PR_ERR_INVALID_ARG for count outside
- * (4096, 2^24] or spin_limit outside [1, 2^20], PR_ERR_OOM or PR_ERR_CUDA.
+ * (8192, 2^24] (more than one 8,192-element tile) or spin_limit outside
+ * [1, 2^20], PR_ERR_OOM or PR_ERR_CUDA.
  * Synchronises `stream`; the CUDA context stays usable.
  */
 pr_status pr_test_scan_timeout(int64_t count, int32_t spin_limit, void *stream);

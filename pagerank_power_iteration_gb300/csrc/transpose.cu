@@ -610,7 +610,7 @@ __global__ void k_tile_rows(const int64_t *__restrict__ row_ptr, int64_t n, int6
 
 // ---------------------------------------------------------------- step 4 --
 
-constexpr int kScanItems = 16;
+constexpr int kScanItems = 32;
 constexpr int kScanTile = kBlock * kScanItems;
 
 struct LoadCount {   // element i of an int32 array

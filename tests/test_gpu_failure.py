@@ -121,7 +121,7 @@ def test_a_look_back_wait_that_runs_out_returns_timeout():
 
 
 def test_the_probe_without_a_withheld_wait_is_refused_on_the_host():
-    for count, spins in ((4096, 10), (0, 10), (1 << 25, 10), (10000, 0), (10000, 1 << 21)):
+    for count, spins in ((8192, 10), (0, 10), (1 << 25, 10), (10000, 0), (10000, 1 << 21)):
         st = prg.pr_test_scan_timeout(count, spins, None)
         assert st == prg.PR_ERR_INVALID_ARG, (count, spins)
 
