@@ -253,6 +253,42 @@ def test_warm_start(dtype):
     assert_ranks_close(xh.cpu().numpy(), ref["x"], tol, "host x_init")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+def test_isolated_vertices(dtype):
+    """Vertices with neither in- nor out-edges are combined row by row in the
+    first update only; later updates count them as n_iso equal terms and the
+    output gives them the last constant term. Half the vertices here are
+    isolated; a warm start gives them arbitrary first values, so the first
+    update's L1 and dangling terms differ per vertex. Every count of updates
+    must match the oracle, and each isolated rank must be the constant term
+    (1-d)/n + d D/n of the last update."""
+    n = 6001
+    rng = np.random.default_rng(21)
+    live = rng.permutation(n)[: n // 2]
+    src = rng.choice(live, size=20000)
+    dst = rng.choice(live, size=20000)
+    rp, ci = gg.from_edges(n, src, dst)
+    outdeg, indeg = np.diff(rp), np.bincount(ci, minlength=n)
+    iso = (outdeg == 0) & (indeg == 0)
+    assert iso.sum() >= n // 2
+    tt = {"f32": torch.float32, "f64": torch.float64}[dtype]
+    tolset = F32 if dtype == "f32" else F64
+    x0 = rng.random(n)
+    x0 /= x0.sum()
+    with prg.Graph(rp, ci) as g:
+        for k in (1, 2, 3, 10):
+            for start in (None, x0):
+                xi = None if start is None else torch.tensor(start, dtype=tt, device="cuda")
+                x, it, l1, _ = g.run(D, 0.0, k, dtype=tt, x_init=xi)
+                x = x.cpu().numpy()
+                ref = oracle.pagerank(rp, ci, D, tol=0.0, max_iter=k,
+                                      **({} if start is None else {"x_init": start}))
+                assert_ranks_close(x, ref["x"], tolset, f"k={k} warm={start is not None}")
+                l1_floor = 4 * 2.0 ** -23 if dtype == "f32" else 1e-12
+                assert abs(l1 - ref["l1"]) <= max(0.02 * ref["l1"], l1_floor)
+                assert np.all(x[iso] == x[iso][0])   # one constant term for all of them
+
+
 def test_host_and_device_buffers_agree():
     rp, ci = graph("rmat14")
     with prg.Graph(rp, ci) as g:                      # host inputs
