@@ -289,6 +289,23 @@ def test_isolated_vertices(dtype):
                 assert np.all(x[iso] == x[iso][0])   # one constant term for all of them
 
 
+def test_precisions_alternate_on_one_handle():
+    """The fp32 state is made with the handle and the fp64 state on the first
+    fp64 run; runs of the two precisions share the handle's scalars. Runs that
+    alternate must each equal the same run on a fresh handle, bit for bit."""
+    rp, ci = graph("rmat14")
+    fresh = {}
+    for tt in (torch.float32, torch.float64):
+        with prg.Graph(rp, ci) as g:
+            fresh[tt] = g.run(D, 1e-6, 200, dtype=tt)
+    with prg.Graph(rp, ci) as g:
+        for tt in (torch.float32, torch.float64, torch.float32, torch.float64, torch.float32):
+            x, it, l1, conv = g.run(D, 1e-6, 200, dtype=tt)
+            fx, fit, fl1, fconv = fresh[tt]
+            assert it == fit and l1 == fl1 and conv == fconv
+            assert torch.equal(x, fx)
+
+
 def test_host_and_device_buffers_agree():
     rp, ci = graph("rmat14")
     with prg.Graph(rp, ci) as g:                      # host inputs
