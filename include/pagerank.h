@@ -206,7 +206,10 @@ pr_status pr_graph_create_ex(int64_t n, int64_t m, const int64_t *row_ptr,
  *   ranks_out  n values of dtype, written with the final ranks
  *              (caller-owned, host or device)
  *   x_init     NULL for the uniform start 1/n, else n values of dtype used
- *              as the start vector (warm start); not renormalised
+ *              as the start vector (warm start); not renormalised. It must be
+ *              a probability vector (every value >= 0, sum 1 up to rounding):
+ *              the L1 and dangling-mass totals are exact fixed-point sums
+ *              sized for totals of at most 2
  *   iters_out  optional (NULL): number of updates performed
  *   l1_out     optional (NULL): L1 distance of the last update
  * The whole loop runs on the device; the call synchronises `stream` once,
