@@ -345,7 +345,8 @@ class Graph:
 
         ``ranks`` is ``out`` if given (host or device tensor/array of ``dtype``)
         or a new CUDA tensor. ``converged`` is False when tol > 0 and
-        max_iter updates did not reach L1 < tol.
+        max_iter updates did not reach L1 < tol. ``x_init`` (warm start) must
+        be a probability vector: non-negative, summing to 1.
         """
         import torch
         dtype = torch.float32 if dtype is None else dtype
